@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for MALA: the planted-peak attention workloads.
+
+This module only draws numbers; it holds none of the attention arithmetic.
+Both the CUDA library's callers and the CPU oracle's tests take their inputs
+from here.
+
+The generator plants, for each query position i, a few "target" keys drawn
+uniformly from its causal prefix [0, i] and sets
+    q_i = A * mean(k_targets) + N(0, 1)
+so each query row has a few large scores above a Gaussian background.  Two
+logit biases are folded into the last head-dim coordinate, because the
+operator takes only q, k and v:
+    q[..., d-1] = 16,   k[j, d-1] = (sink * [j == 0] + c * j) * sqrt(d) / 16,
+which adds  sink * [j == 0] + c * j  to the score of key j under the softmax
+scale 1/sqrt(d).  The recency bias -c (i - j) differs from that by the
+row-constant -c * i, which changes neither the softmax nor any contribution
+test.  Planted terms and noise use coordinates 0 .. d-2.
+
+Large tensors are drawn in fixed-size chunks, each from its own child of the
+seed's SeedSequence, on a thread pool; the values do not depend on the number
+of threads.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+_CHUNK = 1 << 22  # elements per independently seeded chunk
+
+
+def _normal(seed_seq: np.random.SeedSequence, n: int) -> np.ndarray:
+    """n standard normals (float32), drawn chunk-wise in parallel."""
+    out = np.empty(n, dtype=np.float32)
+    nchunks = -(-n // _CHUNK)
+    children = seed_seq.spawn(nchunks)
+
+    def work(c):
+        a = c * _CHUNK
+        b = min(n, a + _CHUNK)
+        np.random.default_rng(children[c]).standard_normal(b - a, dtype=np.float32, out=out[a:b])
+
+    workers = min(32, os.cpu_count() or 1, nchunks)
+    if workers <= 1:
+        for c in range(nchunks):
+            work(c)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+def _round(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
+    """Round-to-nearest-even into ``dtype`` (torch's conversion)."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dtype)
+
+
+@dataclass
+class PrefillConfig:
+    """One prefill (forward + backward) workload."""
+    name: str
+    B: int
+    H: int            # query heads
+    Hkv: int          # key/value heads
+    L: int
+    d: int
+    block: int        # B_q = B_k
+    dtype: torch.dtype
+    n_targets: int
+    amplitude: tuple  # one value, or one per head (drawn from this set per head)
+    sink: float
+    recency: float    # c in the bias -c (i - j)
+    taus: tuple = (1.0,)
+    seed: int = 0
+
+
+@dataclass
+class DecodeConfig:
+    """One split-KV decode workload (a single new query per sequence)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    N: int            # cache length, including the current token
+    d: int
+    block: int
+    num_splits: int
+    dtype: torch.dtype
+    n_targets: int
+    amplitude: float
+    taus: tuple = (1.0, 0.0)
+    seed: int = 0
+
+
+# The five workloads: a tiny fp32 case, then 8K, 32K and 128K bf16 prefill,
+# then 128K bf16 decode with grouped-query heads (4 query heads per KV head).
+CONFIGS = {
+    "tiny_fp32": PrefillConfig("tiny_fp32", 1, 2, 2, 256, 64, 64, torch.float32, 3, (4.0,), 3.0, 0.0, (1.0,), 1001),
+    "prefill_8k": PrefillConfig("prefill_8k", 1, 16, 16, 8192, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.002, (1.0,), 1002),
+    "prefill_32k": PrefillConfig("prefill_32k", 1, 8, 8, 32768, 128, 128, torch.bfloat16, 3, (2.0, 4.0, 8.0), 3.0, 0.002, (1.0, 0.0), 1003),
+    "prefill_128k": PrefillConfig("prefill_128k", 1, 8, 8, 131072, 128, 128, torch.bfloat16, 5, (6.0,), 3.0, 1e-4, (1.0, 0.0), 1004),
+    "decode_128k": DecodeConfig("decode_128k", 8, 32, 8, 131072, 128, 128, 16, torch.bfloat16, 4, 6.0, (1.0, 0.0), 1005),
+}
+
+
+def _head_amplitudes(rng: np.random.Generator, amplitude: tuple, h: int) -> np.ndarray:
+    if len(amplitude) == 1:
+        return np.full(h, float(amplitude[0]))
+    return rng.choice(np.asarray(amplitude, dtype=np.float64), size=h)
+
+
+def prefill_inputs(cfg: PrefillConfig, L: int | None = None, seed: int | None = None,
+                   with_do: bool = True) -> dict:
+    """Planted-peak q, k, v (and dO ~ N(0, 1)) in BSHD layout on the CPU.
+
+    ``L`` overrides the sequence length (same recipe, e.g. for ragged-tail
+    cases); ``seed`` overrides the config's seed.
+    """
+    L = cfg.L if L is None else L
+    seed = cfg.seed if seed is None else seed
+    B, H, Hkv, d = cfg.B, cfg.H, cfg.Hkv, cfg.d
+    ss = np.random.SeedSequence(seed)
+    s_k, s_v, s_noise, s_tgt, s_amp, s_do = ss.spawn(6)
+    k = _normal(s_k, B * L * Hkv * d).reshape(B, L, Hkv, d)
+    v = _normal(s_v, B * L * Hkv * d).reshape(B, L, Hkv, d)
+    amp = _head_amplitudes(np.random.default_rng(s_amp), cfg.amplitude, H)
+    q = _normal(s_noise, B * L * H * d).reshape(B, L, H, d)
+    rng_t = np.random.default_rng(s_tgt)
+    grp = H // Hkv
+    pos = np.arange(L)
+    for b in range(B):
+        for h in range(H):
+            # n_targets keys per query, uniform over the causal prefix [0, i]
+            tgt = np.floor(rng_t.random((L, cfg.n_targets)) * (pos[:, None] + 1)).astype(np.int64)
+            kk = k[b, :, h // grp, : d - 1]
+            mean_t = kk[tgt].mean(axis=1)
+            q[b, :, h, : d - 1] += (amp[h] * mean_t).astype(np.float32)
+    q[..., d - 1] = 16.0
+    k[:, :, :, d - 1] = ((cfg.sink * (pos == 0) + cfg.recency * pos) * math.sqrt(d) / 16.0)[None, :, None]
+    out = {
+        "q": _round(q, cfg.dtype), "k": _round(k, cfg.dtype), "v": _round(v, cfg.dtype),
+        "amplitude": amp, "L": L, "seed": seed,
+    }
+    if with_do:
+        out["do"] = _round(_normal(s_do, B * L * H * d).reshape(B, L, H, d), cfg.dtype)
+    return out
+
+
+def decode_inputs(cfg: DecodeConfig, N: int | None = None, B: int | None = None,
+                  seed: int | None = None) -> dict:
+    """Cache k, v ~ N(0, 1) [B, N, Hkv, d]; each query head
+    q = A * mean(4 random cache keys of its KV head) + N(0, 1); q is [B, H, d]."""
+    N = cfg.N if N is None else N
+    B = cfg.B if B is None else B
+    seed = cfg.seed if seed is None else seed
+    H, Hkv, d = cfg.H, cfg.Hkv, cfg.d
+    ss = np.random.SeedSequence(seed)
+    s_k, s_v, s_noise, s_tgt = ss.spawn(4)
+    k = _normal(s_k, B * N * Hkv * d).reshape(B, N, Hkv, d)
+    v = _normal(s_v, B * N * Hkv * d).reshape(B, N, Hkv, d)
+    q = _normal(s_noise, B * H * d).reshape(B, H, d)
+    rng_t = np.random.default_rng(s_tgt)
+    grp = H // Hkv
+    for b in range(B):
+        for h in range(H):
+            tgt = rng_t.integers(0, N, size=cfg.n_targets)
+            q[b, h] += (cfg.amplitude * k[b, tgt, h // grp].mean(axis=0)).astype(np.float32)
+    return {"q": _round(q, cfg.dtype), "k": _round(k, cfg.dtype), "v": _round(v, cfg.dtype),
+            "N": N, "B": B, "seed": seed}

@@ -1,0 +1,466 @@
+"""fp64 CPU oracle for MassAlloc Attention (MALA).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import or call this
+module: only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline leg use it.  It shares no code with the CUDA library.
+
+Everything here is written to be checked by eye against the pages:
+
+* "MassAlloc Attention: Let Attention Allocate Its Own Compute" (arXiv HTML):
+  §2.1 (score discovery, visible-key counts L_q, threshold tau/L_q),
+  §2.2 Eq. (1)-(4) (online forward test, offline backward test, support
+  nesting), Algorithm 1 (forward), Algorithm 2 (backward), App. A.1 (fused
+  forward/backward/decoding execution, split-KV), App. B Eq. (5)-(10)
+  (omitted-mass bound), App. C.2 (omitted-mass measurement).
+* "Why exact attention does not need a quadratic matrix": Method/Mechanism
+  (block summary (m, l, u) and the merge identity), Example 1.
+
+Conventions (one head at a time; the *_bshd wrappers loop over batch/heads):
+  q [Nq, d], k/v [Nk, d], all float64.  Scores are s = scale * q k^T with the
+  softmax scale applied to the scores (the paper absorbs it into Q, §2.1).
+  Natural exp/log throughout (§2.1).  Zero-based positions; causal prefill
+  means key k is visible to query q iff k <= q, so L_q = q + 1 (§2.1).
+
+Readings of points the pages leave open (each also listed in the design notes):
+  * only key blocks with at least one legal entry for the query block are
+    visited (Algorithm 1 loops over all j; App. A.1 says "legal key blocks");
+  * rows (or entries) that are out of range or fully masked in a tile do not
+    constrain the test (§2.2 text after Eq. 3 and after Eq. 4);
+  * the skip test is a strict "<"; equality retains;
+  * l = 0 is an explicit "+inf ratio, retain" branch (§2.2, first-tile rule);
+  * tau = 0 runs no test at all (dense, §2.3 "tau -> 0 recovers FullAttn");
+  * decode: the query block is the group of query heads sharing one KV head,
+    the split partition is num_splits equal ranges of whole tiles, tiles are
+    visited newest to oldest inside a split, and L = N_k (§2.1, App. A.1).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+__all__ = [
+    "visible_key_counts", "dense_attention", "dense_attention_grads",
+    "restricted_attention", "mala_forward", "mala_backward",
+    "block_summary", "merge_summaries", "mala_decode",
+    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd",
+    "omitted_mass", "BORDERLINE_REL",
+]
+
+# A tile whose largest contribution ratio lies within this relative distance
+# of tau/L_q is "borderline": fp32 and fp64 evaluations may legitimately
+# decide it differently.
+BORDERLINE_REL = 1e-3
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def visible_key_counts(n_q: int, n_k: int, causal: bool) -> np.ndarray:
+    """L_q = |C_q| (§2.1): q + 1 for zero-based causal rows, else N_k."""
+    if causal:
+        return np.arange(1, n_q + 1, dtype=np.float64)
+    return np.full(n_q, float(n_k))
+
+
+def _scores(q, k, scale, rows, cols, causal):
+    """Score tile S = scale * Q_rows K_cols^T with causal entries set to -inf."""
+    s = scale * (q[rows] @ k[cols].T)
+    if causal:
+        s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+    return s
+
+
+# ---------------------------------------------------------------------------
+# Dense causal softmax attention and its analytic gradients (the tau = 0 case).
+# ---------------------------------------------------------------------------
+
+def dense_attention(q, k, v, scale, causal=True, rows=None):
+    """Plain softmax attention: o_q = sum_k p_qk v_k, lse_q = log sum_k exp(s_qk).
+
+    Row-independent, so rows may be evaluated in any order or subset.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(k.shape[0])
+    o = np.zeros((len(rows), v.shape[1]))
+    lse = np.zeros(len(rows))
+    for a in range(0, len(rows), 256):
+        r = rows[a:a + 256]
+        s = _scores(q, k, scale, r, cols, causal)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        z = p.sum(axis=1, keepdims=True)
+        o[a:a + 256] = (p @ v) / z
+        lse[a:a + 256] = (m + np.log(z))[:, 0]
+    return o, lse
+
+
+def dense_attention_grads(q, k, v, do, scale, causal=True):
+    """Analytic softmax-attention gradients w.r.t. the unscaled q, k and v.
+
+    P = softmax(S), dV = P^T dO, dP = dO V^T, D = rowsum(dO o O),
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    rows = np.arange(q.shape[0])
+    cols = np.arange(k.shape[0])
+    s = _scores(q, k, scale, rows, cols, causal)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    p /= p.sum(axis=1, keepdims=True)
+    o = p @ v
+    dv = p.T @ do
+    dp = do @ v.T
+    dd = (do * o).sum(axis=1, keepdims=True)
+    ds = p * (dp - dd)
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv
+
+
+def restricted_attention(q, k, v, scale, keep, bq, bk, causal=True, rows=None):
+    """Softmax attention renormalised over the kept tiles only (§2.2: "the
+    final output is ordinary softmax attention renormalized over the retained
+    tiles").  keep[i, j] says whether tile (query block i, key block j) is kept.
+    Written directly as a masked softmax, with no online update.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nq, nk = q.shape[0], k.shape[0]
+    rows = np.arange(nq) if rows is None else np.asarray(rows)
+    cols = np.arange(nk)
+    s = _scores(q, k, scale, rows, cols, causal)
+    kept = np.asarray(keep, dtype=bool)[(rows // bq)[:, None], (cols // bk)[None, :]]
+    s = np.where(kept, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    z = p.sum(axis=1, keepdims=True)
+    return (p @ v) / z, (m + np.log(z))[:, 0]
+
+
+def omitted_mass(lse_screened, lse_reference):
+    """App. C.2: 1 - exp(l_screened - l_reference), the dense-softmax mass of
+    the positions the screened operator omitted."""
+    return 1.0 - np.exp(_f64(lse_screened) - _f64(lse_reference))
+
+
+# ---------------------------------------------------------------------------
+# MALA forward: Algorithm 1 with the online test of §2.2 Eq. (2)-(3).
+# ---------------------------------------------------------------------------
+
+@dataclass
+class MalaForward:
+    o: np.ndarray          # [Nq, d]
+    lse: np.ndarray        # [Nq] final log-normaliser m + log l (natural log)
+    retained: np.ndarray   # [Tr, Tc] bool: post-score path executed
+    legal: np.ndarray      # [Tr, Tc] bool: tile has >= 1 legal entry (visited)
+    margin: np.ndarray     # [Tr, Tc] max over rows of (log-ratio - log(tau/L)); skip iff < 0
+
+
+def _log_threshold(tau, lq):
+    return math.log(tau) - np.log(lq)
+
+
+def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
+    """MALA forward for one head (Algorithm 1).
+
+    For each query block, legal key blocks are visited from the diagonal
+    toward earlier keys (App. A.1).  For each tile the scores are formed
+    first; the tile is skipped iff for every row with a legal entry in it
+    rowmax(S) - m - log(l) < log(tau / L_q)  (Eq. 3), where a row with l = 0
+    has ratio +inf and therefore retains (§2.2).  A skipped tile leaves
+    (m, l, O) untouched; a retained one takes the standard online-softmax
+    update.  Finalisation: O /= l and lse = m + log(l).
+    ``query_blocks`` restricts the work to a subset of blocks (others stay 0).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if tau < 0 or not np.isfinite(tau):
+        raise ValueError("tau must be finite and >= 0")
+    nq, nk = q.shape[0], k.shape[0]
+    tr, tc = -(-nq // bq), -(-nk // bk)
+    lvis = visible_key_counts(nq, nk, causal)
+    o = np.zeros((nq, v.shape[1]))
+    lse = np.full(nq, np.nan)
+    retained = np.zeros((tr, tc), dtype=bool)
+    legal = np.zeros((tr, tc), dtype=bool)
+    margin = np.full((tr, tc), np.nan)
+    blocks = range(tr) if query_blocks is None else query_blocks
+    for i in blocks:
+        rows = np.arange(i * bq, min(nq, (i + 1) * bq))
+        m = np.full(len(rows), -np.inf)
+        l = np.zeros(len(rows))
+        acc = np.zeros((len(rows), v.shape[1]))
+        thr = _log_threshold(tau, lvis[rows]) if tau > 0 else None
+        for j in reversed(range(tc)):
+            cols = np.arange(j * bk, min(nk, (j + 1) * bk))
+            s = _scores(q, k, scale, rows, cols, causal)
+            has = np.isfinite(s).any(axis=1)      # rows with a legal entry here
+            if not has.any():
+                continue                          # fully masked: not a legal tile
+            legal[i, j] = True
+            mt = np.where(has, s.max(axis=1), -np.inf)
+            if tau > 0:
+                with np.errstate(divide="ignore"):
+                    ratio = np.where(l > 0, mt - m - np.log(np.where(l > 0, l, 1.0)), np.inf)
+                gap = (ratio - thr)[has]
+                margin[i, j] = gap.max()
+                if np.all(gap < 0):
+                    continue                      # skip block (i, j)
+            retained[i, j] = True
+            # online-softmax update; rows without a legal key here keep their state
+            m_new = np.where(has, np.maximum(m, mt), m)
+            alpha = np.ones(len(rows))            # exp(m - m_new); empty rows have nothing to rescale
+            live = l > 0
+            alpha[live] = np.exp(m[live] - m_new[live])
+            p = np.zeros_like(s)
+            p[has] = np.exp(s[has] - m_new[has][:, None])
+            l = alpha * l + p.sum(axis=1)
+            acc = alpha[:, None] * acc + p @ v[cols]
+            m = m_new
+        o[rows] = acc / l[:, None]
+        lse[rows] = m + np.log(l)
+    return MalaForward(o, lse, retained, legal, margin)
+
+
+# ---------------------------------------------------------------------------
+# MALA backward: Algorithm 2 with the offline test of §2.2 Eq. (4).
+# ---------------------------------------------------------------------------
+
+@dataclass
+class MalaBackward:
+    dq: np.ndarray
+    dk: np.ndarray
+    dv: np.ndarray
+    retained: np.ndarray   # [Tr, Tc] bool (indexed [query block, key block])
+    legal: np.ndarray
+    margin: np.ndarray     # max over valid entries of (S - lse - log(tau/L)); skip iff < 0
+
+
+def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=None):
+    """MALA backward for one head (Algorithm 2), key-major.
+
+    For each key block j, the query blocks i with a legal entry are visited in
+    ascending order.  The recomputed tile S_ji is skipped iff
+    S_ji - lse_i^T < log(tau / L_i)^T for every valid causal entry (Eq. 4).
+    A retained tile executes P = exp(S - lse), dP = V dO^T,
+    dS = P o (dP - rowsum(O o dO)), dV += P dO, dK += dS Q, dQ += dS^T K,
+    with the softmax scale carried onto dQ and dK (gradients are w.r.t. the
+    unscaled q and k).  ``tiles`` (a predicate on (i, j)) restricts the work
+    to a subset of tiles, for sampled checks at large sizes.
+    """
+    q, k, v, o, do, lse = (_f64(x) for x in (q, k, v, o, do, lse))
+    if tau < 0 or not np.isfinite(tau):
+        raise ValueError("tau must be finite and >= 0")
+    nq, nk = q.shape[0], k.shape[0]
+    tr, tc = -(-nq // bq), -(-nk // bk)
+    lvis = visible_key_counts(nq, nk, causal)
+    dd = (o * do).sum(axis=1)                     # D = rowsum(O o dO)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    retained = np.zeros((tr, tc), dtype=bool)
+    legal = np.zeros((tr, tc), dtype=bool)
+    margin = np.full((tr, tc), np.nan)
+    for j in range(tc):
+        cols = np.arange(j * bk, min(nk, (j + 1) * bk))
+        for i in range(tr):
+            if tiles is not None and not tiles(i, j):
+                continue
+            rows = np.arange(i * bq, min(nq, (i + 1) * bq))
+            st = _scores(q, k, scale, rows, cols, causal).T     # S_ji = K_j Q_i^T
+            valid = np.isfinite(st)
+            if not valid.any():
+                continue
+            legal[i, j] = True
+            if tau > 0:
+                thr = _log_threshold(tau, lvis[rows])
+                gap = (st - lse[rows][None, :] - thr[None, :])[valid]
+                margin[i, j] = gap.max()
+                if np.all(gap < 0):
+                    continue                                     # skip block (j, i)
+            retained[i, j] = True
+            p = np.where(valid, np.exp(st - lse[rows][None, :]), 0.0)
+            dp = v[cols] @ do[rows].T
+            ds = p * (dp - dd[rows][None, :])
+            dv[cols] += p @ do[rows]
+            dk[cols] += scale * (ds @ q[rows])
+            dq[rows] += scale * (ds.T @ k[cols])
+    return MalaBackward(dq, dk, dv, retained, legal, margin)
+
+
+# ---------------------------------------------------------------------------
+# Block summaries and the exact merge ("Why exact attention does not need a
+# quadratic matrix", Method/Mechanism).
+# ---------------------------------------------------------------------------
+
+def block_summary(scores, values):
+    """(m, l, u) of one non-empty block of finite scores for one query:
+    m = max s, l = sum exp(s - m), u = sum exp(s - m) v."""
+    s = _f64(scores)
+    vals = _f64(values)
+    m = s.max()
+    w = np.exp(s - m)
+    return m, w.sum(), (w[:, None] * vals.reshape(len(s), -1)).sum(axis=0)
+
+
+def merge_summaries(summaries):
+    """Merge identity: m = max m_b; rescale each (l_b, u_b) by exp(m_b - m)
+    and add.  Empty blocks (l = 0, e.g. fully masked) carry no weight and are
+    left out explicitly rather than evaluating -inf - (-inf)."""
+    live = [(m, l, u) for (m, l, u) in summaries if l > 0]
+    if not live:
+        raise ValueError("merge of empty blocks only")
+    m = max(mb for mb, _, _ in live)
+    l = sum(math.exp(mb - m) * lb for mb, lb, _ in live)
+    u = sum(math.exp(mb - m) * np.asarray(ub, dtype=np.float64) for mb, _, ub in live)
+    return m, l, u
+
+
+# ---------------------------------------------------------------------------
+# MALA split-KV decode (App. A.1 "Fused decoding execution", §2.4).
+# ---------------------------------------------------------------------------
+
+@dataclass
+class MalaDecode:
+    o: np.ndarray          # [G, d]
+    lse: np.ndarray        # [G]
+    retained: np.ndarray   # [T] bool per key tile
+    margin: np.ndarray     # [T]
+    summaries: list        # per split: (m [G], l [G], u [G, d])
+
+
+def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
+    """One query position of G query heads sharing one KV head, against an
+    N-token cache (the cache already holds the current token, so L = N).
+
+    The T = ceil(N / bk) key tiles are cut into ``num_splits`` contiguous
+    ranges of ceil(T / num_splits) whole tiles.  Each split starts from its
+    own empty (m, l) and visits its tiles newest to oldest, scoring every
+    tile; a tile is skipped iff rowmax - m - log l < log(tau / N) holds for
+    all G rows (Eq. 3 with the group of heads as the query block, l = 0 =>
+    retain).  The splits' (m, l, u) are merged with the exact identity.
+    """
+    qg, kc, vc = _f64(qg), _f64(kc), _f64(vc)
+    if tau < 0 or not np.isfinite(tau):
+        raise ValueError("tau must be finite and >= 0")
+    g, n = qg.shape[0], kc.shape[0]
+    t = -(-n // bk)
+    per = -(-t // num_splits)
+    thr = math.log(tau) - math.log(n) if tau > 0 else None
+    retained = np.zeros(t, dtype=bool)
+    margin = np.full(t, np.nan)
+    summaries = []
+    for sp in range(num_splits):
+        m = np.full(g, -np.inf)
+        l = np.zeros(g)
+        u = np.zeros((g, vc.shape[1]))
+        for j in reversed(range(sp * per, min(t, (sp + 1) * per))):
+            cols = np.arange(j * bk, min(n, (j + 1) * bk))
+            s = scale * (qg @ kc[cols].T)
+            mt = s.max(axis=1)
+            if tau > 0:
+                with np.errstate(divide="ignore"):
+                    ratio = np.where(l > 0, mt - m - np.log(np.where(l > 0, l, 1.0)), np.inf)
+                gap = ratio - thr
+                margin[j] = gap.max()
+                if np.all(gap < 0):
+                    continue
+            retained[j] = True
+            m_new = np.maximum(m, mt)
+            alpha = np.ones(g)                    # exp(m - m_new); an empty state has nothing to rescale
+            live = l > 0
+            alpha[live] = np.exp(m[live] - m_new[live])
+            p = np.exp(s - m_new[:, None])
+            l = alpha * l + p.sum(axis=1)
+            u = alpha[:, None] * u + p @ vc[cols]
+            m = m_new
+        summaries.append((m, l, u))
+    o = np.zeros((g, vc.shape[1]))
+    lse = np.zeros(g)
+    for r in range(g):
+        mr, lr, ur = merge_summaries([(m[r], l[r], u[r]) for (m, l, u) in summaries])
+        o[r] = ur / lr
+        lse[r] = mr + math.log(lr)
+    return MalaDecode(o, lse, retained, margin, summaries)
+
+
+# ---------------------------------------------------------------------------
+# Batched wrappers over the library's layouts (BSHD for prefill, GQA mapping
+# query head h -> KV head h // (Hq / Hkv)).
+# ---------------------------------------------------------------------------
+
+def mala_forward_bshd(q, k, v, scale, tau, bq, bk, causal=True, heads=None,
+                      batches=None, query_blocks=None):
+    """q [B, L, Hq, d], k/v [B, L, Hkv, d] -> dict of o [B, L, Hq, d],
+    lse [B, Hq, L], retained/legal/margin [B, Hq, Tr, Tc]."""
+    bsz, nq, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    grp = hq // hkv
+    tr, tc = -(-nq // bq), -(-nk // bk)
+    out = {
+        "o": np.zeros((bsz, nq, hq, v.shape[3])),
+        "lse": np.full((bsz, hq, nq), np.nan),
+        "retained": np.zeros((bsz, hq, tr, tc), dtype=bool),
+        "legal": np.zeros((bsz, hq, tr, tc), dtype=bool),
+        "margin": np.full((bsz, hq, tr, tc), np.nan),
+    }
+    for b in (range(bsz) if batches is None else batches):
+        for h in (range(hq) if heads is None else heads):
+            r = mala_forward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], scale, tau,
+                             bq, bk, causal, query_blocks)
+            out["o"][b, :, h] = r.o
+            out["lse"][b, h] = r.lse
+            out["retained"][b, h] = r.retained
+            out["legal"][b, h] = r.legal
+            out["margin"][b, h] = r.margin
+    return out
+
+
+def mala_backward_bshd(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, heads=None,
+                       batches=None, tiles=None):
+    """Gradients for BSHD inputs; dk/dv of a KV head sum over its query heads."""
+    bsz, nq, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    grp = hq // hkv
+    tr, tc = -(-nq // bq), -(-nk // bk)
+    out = {
+        "dq": np.zeros(q.shape), "dk": np.zeros(k.shape), "dv": np.zeros(v.shape),
+        "retained": np.zeros((bsz, hq, tr, tc), dtype=bool),
+        "legal": np.zeros((bsz, hq, tr, tc), dtype=bool),
+        "margin": np.full((bsz, hq, tr, tc), np.nan),
+    }
+    for b in (range(bsz) if batches is None else batches):
+        for h in (range(hq) if heads is None else heads):
+            r = mala_backward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], o[b, :, h],
+                              do[b, :, h], lse[b, h], scale, tau, bq, bk, causal, tiles)
+            out["dq"][b, :, h] = r.dq
+            out["dk"][b, :, h // grp] += r.dk
+            out["dv"][b, :, h // grp] += r.dv
+            out["retained"][b, h] = r.retained
+            out["legal"][b, h] = r.legal
+            out["margin"][b, h] = r.margin
+    return out
+
+
+def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None):
+    """q [B, Hq, d], caches [B, N, Hkv, d] -> o [B, Hq, d], lse [B, Hq],
+    retained/margin [B, Hkv, T]."""
+    bsz, hq, d = q.shape
+    n, hkv = k_cache.shape[1], k_cache.shape[2]
+    grp = hq // hkv
+    t = -(-n // bk)
+    o = np.zeros((bsz, hq, v_cache.shape[3]))
+    lse = np.full((bsz, hq), np.nan)
+    retained = np.zeros((bsz, hkv, t), dtype=bool)
+    margin = np.full((bsz, hkv, t), np.nan)
+    for b in (range(bsz) if batches is None else batches):
+        for hk in range(hkv):
+            r = mala_decode(q[b, hk * grp:(hk + 1) * grp], k_cache[b, :, hk], v_cache[b, :, hk],
+                            scale, tau, bk, num_splits)
+            o[b, hk * grp:(hk + 1) * grp] = r.o
+            lse[b, hk * grp:(hk + 1) * grp] = r.lse
+            retained[b, hk] = r.retained
+            margin[b, hk] = r.margin
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin}

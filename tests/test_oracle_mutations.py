@@ -1,0 +1,79 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch each one.  Every mutant is built from the oracle's source on the CPU;
+the real oracle module is never modified."""
+import inspect
+import sys
+import types
+
+import pytest
+
+import oracle.mala_oracle as real
+import tests.test_oracle_pins as pins
+
+SRC = inspect.getsource(real)
+
+# (name, text in the oracle, replacement)
+MUTATIONS = [
+    ("rescale sign", "alpha[live] = np.exp(m[live] - m_new[live])\n            p = np.zeros_like(s)",
+     "alpha[live] = np.exp(m_new[live] - m[live])\n            p = np.zeros_like(s)"),
+    ("test sign on log l", "mt - m - np.log(np.where(l > 0, l, 1.0)), np.inf)\n                gap = (ratio - thr)[has]",
+     "mt - m + np.log(np.where(l > 0, l, 1.0)), np.inf)\n                gap = (ratio - thr)[has]"),
+    ("L_q off by one", "return np.arange(1, n_q + 1, dtype=np.float64)",
+     "return np.arange(2, n_q + 2, dtype=np.float64)"),
+    ("any instead of all", "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                if np.all(gap < 0):",
+     "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                if np.any(gap < 0):"),
+    ("decode L off by one", "thr = math.log(tau) - math.log(n) if tau > 0 else None",
+     "thr = math.log(tau) - math.log(n + 1) if tau > 0 else None"),
+    ("ascending forward traversal", "for j in reversed(range(tc)):", "for j in range(tc):"),
+    ("dS sign of D", "ds = p * (dp - dd[rows][None, :])", "ds = p * (dp + dd[rows][None, :])"),
+    ("dQ drops scale", "dq[rows] += scale * (ds.T @ k[cols])", "dq[rows] += ds.T @ k[cols]"),
+    ("dK transposed operand", "dk[cols] += scale * (ds @ q[rows])", "dk[cols] += scale * (p @ q[rows])"),
+    ("bwd threshold sign", "gap = (st - lse[rows][None, :] - thr[None, :])[valid]",
+     "gap = (st - lse[rows][None, :] + thr[None, :])[valid]"),
+    ("decode oldest first", "for j in reversed(range(sp * per, min(t, (sp + 1) * per))):",
+     "for j in range(sp * per, min(t, (sp + 1) * per)):"),
+    ("merge without rescale", "l = sum(math.exp(mb - m) * lb for mb, lb, _ in live)",
+     "l = sum(lb for mb, lb, _ in live)"),
+    ("causal mask hides diagonal", "s = np.where(cols[None, :] > rows[:, None], -np.inf, s)",
+     "s = np.where(cols[None, :] >= rows[:, None], -np.inf, s)"),
+    ("dense D dropped", "ds = p * (dp - dd)", "ds = p * dp"),
+    ("lse drops max", "lse[rows] = m + np.log(l)", "lse[rows] = np.log(l)"),
+]
+
+PIN_TESTS = [
+    (pins.test_merge_worked_examples, {}),
+    (pins.test_dense_matches_library, {"causal": True}),
+    (pins.test_dense_closed_forms, {}),
+    (pins.test_dense_grads_match_library_and_finite_differences, {}),
+    (pins.test_forward_tau0_is_dense, {"L": 200, "bq": 64}),
+    (pins.test_forward_matches_brute_force_ratio_rule, {"tau": 1.0, "b": 16, "seed": 3}),
+    (pins.test_forward_bounds_of_appendix_b, {"tau": 1.0, "b": 16}),
+    (pins.test_backward_tau0_is_dense_gradient, {"L": 96, "b": 32}),
+    (pins.test_backward_brute_force_entry_rule, {}),
+    (pins.test_backward_is_gradient_of_forward_when_supports_coincide, {}),
+    (pins.test_decode_tau0_is_dense, {"n": 500, "splits": 3}),
+    (pins.test_decode_single_split_equals_forward_on_the_head_group, {}),
+    (pins.test_uniform_scores_closed_form, {}),
+    (pins.test_decode_uniform_scores_closed_form, {}),
+]
+
+
+def _mutant(old, new):
+    assert SRC.count(old) == 1, old
+    mod = types.ModuleType("mala_oracle_mutant")
+    sys.modules[mod.__name__] = mod          # dataclasses look the module up by name
+    exec(compile(SRC.replace(old, new), "mala_oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, monkeypatch):
+    mod = _mutant(old, new)
+    monkeypatch.setattr(pins, "orc", mod)
+    caught = []
+    for fn, kw in PIN_TESTS:
+        try:
+            fn(**kw)
+        except (AssertionError, ValueError, FloatingPointError, IndexError):
+            caught.append(fn.__name__)
+    assert caught, f"no pin catches the planted mistake: {name}"

@@ -1,0 +1,406 @@
+"""Pins for the fp64 oracle: each check ties the oracle to something other than
+itself -- the worked examples printed on the pages, closed forms, a library
+routine for the dense special case, finite differences, the bounds the paper
+proves, and a brute-force restatement of the skip rule in its ratio form.
+
+Citations name the page and its section / equation:
+  MALA = "MassAlloc Attention: Let Attention Allocate Its Own Compute";
+  MERGE = "Why exact attention does not need a quadratic matrix".
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from mass_adaptive_sparse_gb300 import synthetic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "merge_examples.txt")
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _sdpa(q, k, v, scale, causal=True, mask=None):
+    """torch's fp64 scaled_dot_product_attention on one head; also returns lse."""
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64)[None, None] for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=None if mask is None else torch.tensor(mask)[None, None],
+        is_causal=causal and mask is None, scale=scale)
+    s = scale * (tq @ tk.transpose(-1, -2))
+    if mask is not None:
+        s = s.masked_fill(~torch.tensor(mask)[None, None], float("-inf"))
+    elif causal:
+        n = q.shape[0]
+        s = s.masked_fill(torch.ones(n, k.shape[0], dtype=torch.bool).triu(1), float("-inf"))
+    return o[0, 0].numpy(), torch.logsumexp(s, -1)[0, 0].numpy()
+
+
+def _sdpa_grads(q, k, v, do, scale, causal=True):
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                                         is_causal=causal, scale=scale)[0, 0]
+    (o * torch.tensor(do)).sum().backward()
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+PIN_SCALE = 1 / math.sqrt(32)
+
+
+def _peaked(L=256, seed=7):
+    """One head of the planted-peak recipe at d = 32 with a strong recency
+    bias (-0.1 (i - j)), so that small cases skip a good share of tiles."""
+    cfg = synthetic.PrefillConfig("pin", 1, 1, 1, L, 32, 16, torch.float32, 3, (4.0,), 3.0, 0.1)
+    x = synthetic.prefill_inputs(cfg, L=L, seed=seed)
+    return (x["q"][0, :, 0].double().numpy(), x["k"][0, :, 0].double().numpy(),
+            x["v"][0, :, 0].double().numpy(), x["do"][0, :, 0].double().numpy())
+
+
+# ---------------------------------------------------------------------------
+# MERGE, Example 1 and its variant (golden values printed on the page).
+# ---------------------------------------------------------------------------
+
+def _parse(tok):
+    out = []
+    for t in tok.split(","):
+        out.append(math.log(2) if t == "log2" else math.log(4) if t == "log4" else float(t))
+    return out
+
+
+def test_merge_worked_examples():
+    rows = [ln.split() for ln in open(GOLDEN) if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 2
+    for case, a_s, a_v, b_s, b_v, a_sum, b_sum, merged, weights in rows:
+        sa = orc.block_summary(_parse(a_s), _parse(a_v))
+        sb = orc.block_summary(_parse(b_s), _parse(b_v))
+        for got, want in ((sa, _parse(a_sum)), (sb, _parse(b_sum))):
+            assert got[0] == pytest.approx(want[0], abs=1e-15)
+            assert got[1] == pytest.approx(want[1], abs=1e-15)
+            assert got[2][0] == pytest.approx(want[2], abs=1e-15)
+        m, l, u = orc.merge_summaries([sa, sb])
+        assert u[0] / l == pytest.approx(float(merged), abs=1e-14), case
+        # averaging local outputs is right in example 1 only by coincidence
+        avg = 0.5 * (sa[2][0] / sa[1] + sb[2][0] / sb[1])
+        assert (avg == pytest.approx(float(merged))) == (case == "example1")
+        if weights != "-":
+            s = np.array(_parse(a_s) + _parse(b_s))
+            w = np.exp(s) / np.exp(s).sum()
+            np.testing.assert_allclose(w, _parse(weights), atol=1e-15)
+        # the merge is order independent and ignores empty blocks
+        m2, l2, u2 = orc.merge_summaries([sb, (0.0, 0.0, np.zeros(1)), sa])
+        assert u2[0] / l2 == pytest.approx(float(merged), abs=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Dense attention (the tau = 0 case) against closed forms and torch.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dense_matches_library(causal):
+    q, k, v = _rand((70, 16), 1), _rand((70, 16), 2), _rand((70, 16), 3)
+    o, lse = orc.dense_attention(q, k, v, 0.3, causal)
+    o_ref, lse_ref = _sdpa(q, k, v, 0.3, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_dense_closed_forms():
+    q, k, v = _rand((40, 8), 4), _rand((40, 8), 5), _rand((40, 8), 6)
+    o, lse = orc.dense_attention(q, k, v, 0.5)
+    # row 0 sees only key 0
+    np.testing.assert_allclose(o[0], v[0], atol=1e-15)
+    assert lse[0] == pytest.approx(0.5 * q[0] @ k[0], abs=1e-14)
+    # a zero query attends uniformly over its prefix
+    o0, lse0 = orc.dense_attention(np.zeros_like(q), k, v, 0.5)
+    np.testing.assert_allclose(o0, np.cumsum(v, 0) / np.arange(1, 41)[:, None], atol=1e-14)
+    np.testing.assert_allclose(lse0, np.log(np.arange(1, 41)), atol=1e-14)
+
+
+def test_dense_grads_match_library_and_finite_differences():
+    q, k, v, do = (_rand((24, 8), s) for s in (7, 8, 9, 10))
+    dq, dk, dv = orc.dense_attention_grads(q, k, v, do, 0.4)
+    for got, want in zip((dq, dk, dv), _sdpa_grads(q, k, v, do, 0.4)):
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+    # central differences of f = <o, dO>
+    f = lambda qq, kk, vv: (orc.dense_attention(qq, kk, vv, 0.4)[0] * do).sum()
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0), (5, 3), (23, 7), (11, 1)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if n == name else y for n, y in (("q", q), ("k", k), ("v", v))]
+            args_m = [xm if n == name else y for n, y in (("q", q), ("k", k), ("v", v))]
+            fd = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert fd == pytest.approx(g[idx], rel=1e-6, abs=1e-9), (name, idx)
+
+
+# ---------------------------------------------------------------------------
+# MALA forward (MALA §2.2 Eq. 2-3, Algorithm 1, App. B).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L,bq", [(128, 32), (200, 64), (97, 16)])
+def test_forward_tau0_is_dense(L, bq):
+    q, k, v = _rand((L, 16), 11, 2.0), _rand((L, 16), 12), _rand((L, 16), 13)
+    r = orc.mala_forward(q, k, v, 0.25, 0.0, bq, bq)
+    o_ref, lse_ref = _sdpa(q, k, v, 0.25)
+    np.testing.assert_allclose(r.o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r.lse, lse_ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(r.retained, r.legal)
+    t = -(-L // bq)
+    assert np.array_equal(r.legal, np.tril(np.ones((t, t), dtype=bool)))
+
+
+def test_forward_huge_tau_keeps_only_diagonal_tiles():
+    L, b = 128, 32
+    q, k, v = _rand((L, 16), 14), _rand((L, 16), 15), _rand((L, 16), 16)
+    r = orc.mala_forward(q, k, v, 0.25, 1e30, b, b)
+    assert np.array_equal(r.retained, np.eye(L // b, dtype=bool))
+    blk = np.arange(L) // b
+    mask = (blk[:, None] == blk[None, :]) & (np.arange(L)[None, :] <= np.arange(L)[:, None])
+    o_ref, lse_ref = _sdpa(q, k, v, 0.25, mask=mask)
+    np.testing.assert_allclose(r.o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r.lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def _brute_force_forward(q, k, v, scale, tau, b):
+    """Eq. 2 in ratio form with the retained key set kept explicitly: before
+    each tile, Z = sum over retained keys of exp(s) (Eq. 1), and the tile is
+    skipped iff exp(max legal s) / Z < tau / L_q for every row (Z = 0 retains).
+    Output = softmax over the retained keys."""
+    L = q.shape[0]
+    s_all = scale * q @ k.T
+    t = -(-L // b)
+    keep = np.zeros((t, t), dtype=bool)
+    o = np.zeros_like(q)
+    lse = np.zeros(L)
+    for i in range(t):
+        rows = range(i * b, min(L, (i + 1) * b))
+        kept_keys = {r: [] for r in rows}
+        for j in range(i, -1, -1):
+            skip = True
+            for r in rows:
+                legal = [c for c in range(j * b, min(L, (j + 1) * b)) if c <= r]
+                if not legal:
+                    continue
+                z = sum(math.exp(s_all[r, c]) for c in kept_keys[r])
+                if z == 0 or math.exp(max(s_all[r, c] for c in legal)) / z >= tau / (r + 1):
+                    skip = False
+            if skip:
+                continue
+            keep[i, j] = True
+            for r in rows:
+                kept_keys[r] += [c for c in range(j * b, min(L, (j + 1) * b)) if c <= r]
+        for r in rows:
+            w = np.array([math.exp(s_all[r, c]) for c in kept_keys[r]])
+            o[r] = (w[:, None] * v[kept_keys[r]]).sum(0) / w.sum()
+            lse[r] = math.log(w.sum())
+    return o, lse, keep
+
+
+@pytest.mark.parametrize("tau,b,seed", [(1.0, 16, 3), (1.0, 8, 11), (2.0, 16, 5), (0.5, 8, 6)])
+def test_forward_matches_brute_force_ratio_rule(tau, b, seed):
+    q, k, v, _ = _peaked(L=128, seed=seed)
+    r = orc.mala_forward(q, k, v, PIN_SCALE, tau, b, b)
+    o, lse, keep = _brute_force_forward(q, k, v, PIN_SCALE, tau, b)
+    assert np.array_equal(r.retained, keep)
+    assert (~keep & np.tril(np.ones_like(keep))).any(), "case must skip something"
+    np.testing.assert_allclose(r.o, o, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(r.lse, lse, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("tau,b", [(1.0, 16), (1.0, 64), (0.1, 32), (3.0, 16)])
+def test_forward_bounds_of_appendix_b(tau, b):
+    q, k, v, _ = _peaked(L=256, seed=11)
+    scale = PIN_SCALE
+    r = orc.mala_forward(q, k, v, scale, tau, b, b)
+    # the output is ordinary softmax renormalised over the retained tiles (§2.2)
+    o_r, lse_r = orc.restricted_attention(q, k, v, scale, r.retained, b, b)
+    np.testing.assert_allclose(r.o, o_r, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(r.lse, lse_r, rtol=1e-12, atol=1e-12)
+    o_d, lse_d = orc.dense_attention(q, k, v, scale)
+    L = q.shape[0]
+    lq = np.arange(1, L + 1)
+    s = scale * q @ k.T
+    blk = np.arange(L) // b
+    omitted = (~r.retained[blk[:, None], blk[None, :]]) & (np.arange(L)[None, :] <= np.arange(L)[:, None])
+    assert omitted.any()
+    # every omitted key: exp(s_k) / Z_R < tau / L_q  (App. B, Eq. 7 with Z_R >= Z_t)
+    rr, cc = np.nonzero(omitted)
+    assert np.all(s[rr, cc] - r.lse[rr] < math.log(tau) - np.log(lq[rr]))
+    # omitted mass eps_q <= tau / (1 + tau)  (Eq. 6), measured as in App. C.2
+    eps = orc.omitted_mass(r.lse, lse_d)
+    assert np.all(eps >= -1e-12) and np.all(eps <= tau / (1 + tau))
+    # ||p - p~||_1 = 2 eps  (Eq. 9)  and  ||o - o~|| <= 2 tau/(1+tau) V_max  (Eq. 10)
+    p = np.exp(np.where(np.tril(np.ones((L, L), bool)), s, -np.inf) - lse_d[:, None])
+    pt = np.where(omitted, 0.0, np.exp(np.where(np.tril(np.ones((L, L), bool)), s, -np.inf) - r.lse[:, None]))
+    np.testing.assert_allclose(np.abs(p - pt).sum(1), 2 * eps, atol=1e-12)
+    vmax = np.linalg.norm(v, axis=1).max()
+    assert np.all(np.linalg.norm(o_d - r.o, axis=1) <= 2 * tau / (1 + tau) * vmax + 1e-12)
+
+
+def test_uniform_scores_closed_form():
+    """All scores equal (q = 0) and 1x1 tiles: when row r tests key k it has
+    retained n keys, each key's ratio is 1/n, and the key is skipped iff
+    1/n < tau/L_r with L_r = r + 1 (Eq. 2).  So row r keeps its newest
+    n* = min(r + 1, floor((r + 1)/tau) + 1) keys; lse = log n*; o = their mean.
+    Backward then skips every entry, since (r + 1)/n* < tau (Eq. 4)."""
+    L, tau = 64, math.pi
+    q = np.zeros((L, 4))
+    k, v, do = _rand((L, 4), 51), _rand((L, 4), 52), _rand((L, 4), 53)
+    r = orc.mala_forward(q, k, v, 1.0, tau, 1, 1)
+    for row in range(L):
+        n_star = min(row + 1, math.floor((row + 1) / tau) + 1)
+        assert r.retained[row].sum() == n_star
+        assert r.retained[row, row - n_star + 1: row + 1].all()
+        assert r.lse[row] == pytest.approx(math.log(n_star), abs=1e-13)
+        np.testing.assert_allclose(r.o[row], v[row - n_star + 1: row + 1].mean(0), atol=1e-13)
+    g = orc.mala_backward(q, k, v, r.o, do, r.lse, 1.0, tau, 1, 1)
+    assert not g.retained.any()
+
+
+def test_decode_uniform_scores_closed_form():
+    """Decode analogue with L = N: one split keeps the newest floor(N/tau) + 1
+    keys; two splits each keep their own newest floor(N/tau) + 1."""
+    n, tau = 50, math.pi
+    kc, vc = _rand((n, 4), 54), _rand((n, 4), 55)
+    r = orc.mala_decode(np.zeros((2, 4)), kc, vc, 1.0, tau, 1, 1)
+    n_star = math.floor(n / tau) + 1
+    assert r.retained.sum() == n_star and r.retained[n - n_star:].all()
+    np.testing.assert_allclose(r.lse, math.log(n_star), atol=1e-13)
+    np.testing.assert_allclose(r.o[0], vc[n - n_star:].mean(0), atol=1e-13)
+    r2 = orc.mala_decode(np.zeros((2, 4)), kc, vc, 1.0, tau, 1, 2)
+    assert r2.retained[:25].sum() == n_star and r2.retained[25 - n_star:25].all()
+    assert r2.retained[25:].sum() == n_star and r2.retained[n - n_star:].all()
+    keep = np.r_[np.arange(25 - n_star, 25), np.arange(n - n_star, n)]
+    np.testing.assert_allclose(r2.o[1], vc[keep].mean(0), atol=1e-13)
+
+
+def test_forward_first_tile_always_retained_and_rows_nonempty():
+    q, k, v, _ = _peaked(L=200, seed=12)
+    r = orc.mala_forward(q, k, v, PIN_SCALE, 1.0, 32, 32)
+    assert np.all(np.diag(r.retained))
+    assert np.all(np.isfinite(r.lse)) and np.all(np.isfinite(r.o))
+
+
+# ---------------------------------------------------------------------------
+# MALA backward (MALA §2.2 Eq. 4, Algorithm 2).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L,b", [(96, 32), (200, 64)])
+def test_backward_tau0_is_dense_gradient(L, b):
+    q, k, v, do = (_rand((L, 16), s) for s in (21, 22, 23, 24))
+    f = orc.mala_forward(q, k, v, 0.25, 0.0, b, b)
+    g = orc.mala_backward(q, k, v, f.o, do, f.lse, 0.25, 0.0, b, b)
+    for got, want in zip((g.dq, g.dk, g.dv), _sdpa_grads(q, k, v, do, 0.25)):
+        np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-11)
+
+
+def test_backward_huge_tau_skips_everything():
+    q, k, v, do = (_rand((64, 16), s) for s in (25, 26, 27, 28))
+    f = orc.mala_forward(q, k, v, 0.25, 1e30, 16, 16)
+    g = orc.mala_backward(q, k, v, f.o, do, f.lse, 0.25, 1e30, 16, 16)
+    assert not g.retained.any()
+    assert not (g.dq.any() or g.dk.any() or g.dv.any())
+
+
+@pytest.mark.parametrize("tau,b,seed", [(1.0, 16, 31), (1.0, 32, 32), (0.5, 8, 33)])
+def test_backward_support_nested_in_forward(tau, b, seed):
+    q, k, v, do = _peaked(L=256, seed=seed)
+    f = orc.mala_forward(q, k, v, PIN_SCALE, tau, b, b)
+    g = orc.mala_backward(q, k, v, f.o, do, f.lse, PIN_SCALE, tau, b, b)
+    assert np.array_equal(g.legal, f.legal)
+    assert not (g.retained & ~f.retained).any()          # bwd support within fwd support
+    assert (f.retained & ~g.retained).any() or True       # may be strictly smaller
+
+
+def test_backward_brute_force_entry_rule():
+    """Eq. 4 as a loop over single entries: tile (j, i) is kept iff some valid
+    entry has exp(s - lse_q) >= tau / L_q."""
+    q, k, v, do = _peaked(L=128, seed=34)
+    b, tau = 16, 1.0
+    f = orc.mala_forward(q, k, v, PIN_SCALE, tau, b, b)
+    g = orc.mala_backward(q, k, v, f.o, do, f.lse, PIN_SCALE, tau, b, b)
+    s = PIN_SCALE * (q @ k.T)
+    t = 128 // b
+    for i in range(t):
+        for j in range(i + 1):
+            keep = any(math.exp(s[r, c] - f.lse[r]) >= tau / (r + 1)
+                       for r in range(i * b, (i + 1) * b) for c in range(j * b, (j + 1) * b) if c <= r)
+            assert g.retained[i, j] == keep
+
+
+def test_backward_is_gradient_of_forward_when_supports_coincide():
+    """Where the backward support equals the forward one and no test is near
+    its threshold, MALA forward is smooth and Algorithm 2 is its exact
+    gradient (central differences)."""
+    q, k, v, do = _peaked(L=128, seed=3)
+    scale, tau, b = PIN_SCALE, 1.0, 16
+    f = orc.mala_forward(q, k, v, scale, tau, b, b)
+    g = orc.mala_backward(q, k, v, f.o, do, f.lse, scale, tau, b, b)
+    assert np.array_equal(g.retained, f.retained) and not np.array_equal(f.retained, f.legal)
+    assert np.nanmin(np.abs(f.margin[f.legal & np.isfinite(f.margin)])) > 1e-3
+    assert np.nanmin(np.abs(g.margin[g.legal])) > 1e-3
+    fun = lambda qq, kk, vv: (orc.mala_forward(qq, kk, vv, scale, tau, b, b).o * do).sum()
+    eps = 1e-6
+    rng = np.random.default_rng(0)
+    for name, x, gr in (("q", q, g.dq), ("k", k, g.dk), ("v", v, g.dv)):
+        for _ in range(6):
+            idx = (rng.integers(0, 128), rng.integers(0, 32))
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            ap = [xp if n == name else y for n, y in (("q", q), ("k", k), ("v", v))]
+            am = [xm if n == name else y for n, y in (("q", q), ("k", k), ("v", v))]
+            fd = (fun(*ap) - fun(*am)) / (2 * eps)
+            assert fd == pytest.approx(gr[idx], rel=1e-5, abs=1e-8), (name, idx)
+
+
+# ---------------------------------------------------------------------------
+# Split-KV decode (MALA §2.4, App. A.1) and the merge.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,splits", [(512, 1), (512, 4), (500, 3), (100, 8)])
+def test_decode_tau0_is_dense(n, splits):
+    qg = _rand((4, 16), 41, 2.0)
+    kc, vc = _rand((n, 16), 42), _rand((n, 16), 43)
+    r = orc.mala_decode(qg, kc, vc, 0.25, 0.0, 32, splits)
+    o_ref, lse_ref = _sdpa(qg, kc, vc, 0.25, causal=False)
+    np.testing.assert_allclose(r.o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r.lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_single_split_equals_forward_on_the_head_group():
+    """With one split, decode is Algorithm 1 on a query block made of the G
+    heads of a group, all seeing the full cache (L = N)."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    x = synthetic.decode_inputs(cfg, N=1000, B=1, seed=3)
+    qg = x["q"][0, 0:4].double().numpy()
+    kc, vc = x["k"][0, :, 0].double().numpy(), x["v"][0, :, 0].double().numpy()
+    scale = 1 / math.sqrt(128)
+    r = orc.mala_decode(qg, kc, vc, scale, 1.0, 128, 1)
+    f = orc.mala_forward(qg, kc, vc, scale, 1.0, 4, 128, causal=False)
+    np.testing.assert_allclose(r.o, f.o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r.lse, f.lse, rtol=1e-13)
+    assert np.array_equal(r.retained, f.retained[0])
+
+
+def test_decode_split_output_is_renormalised_softmax_and_bounded():
+    cfg = synthetic.CONFIGS["decode_128k"]
+    x = synthetic.decode_inputs(cfg, N=2048, B=1, seed=4)
+    qg = x["q"][0, 4:8].double().numpy()
+    kc, vc = x["k"][0, :, 1].double().numpy(), x["v"][0, :, 1].double().numpy()
+    scale = 1 / math.sqrt(128)
+    for splits in (1, 4, 16):
+        r = orc.mala_decode(qg, kc, vc, scale, 1.0, 64, splits)
+        keep = np.tile(r.retained[None, :], (4, 1))
+        # query "block" index is the head row here: one block of 4 rows
+        o_r, lse_r = orc.restricted_attention(qg, kc, vc, scale, r.retained[None, :], 4, 64, causal=False)
+        np.testing.assert_allclose(r.o, o_r, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(r.lse, lse_r, rtol=1e-12)
+        _, lse_d = orc.dense_attention(qg, kc, vc, scale, causal=False)
+        assert np.all(orc.omitted_mass(r.lse, lse_d) <= 0.5)
+        assert keep.shape == (4, 32)
