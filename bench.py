@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark of the MALA hot path on GB300.
+
+One step = one pass of the whole path on synthetic planted-peak data:
+  MALA forward + backward on the 128K prefill workload (B=1, 8 query / 8 KV
+  heads, L=131072, d=128, bf16, 128x128 tiles) and one split-KV decode step on
+  the 128K decode workload (batch 8, 32 query / 8 KV heads, 131072-token bf16
+  cache, 16 splits), all at tau = 1.
+The same steps are then timed at tau = 0 (dense, same kernels) for the speedup.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MALA fwd/bwd ms & TFLOP/s at 32K/128K, decode µs/token at 128K; % roofline"
+WORKLOADS = {
+    "128k": ("prefill_128k", "decode_128k"),
+    "32k": ("prefill_32k", "decode_128k"),
+}
+L2_BYTES = 129 * 1024 * 1024
+SMS = 152
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["mala", "reference"], default="mala")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="128k")
+    p.add_argument("--tau", type=float, default=1.0)
+    p.add_argument("--no-dense", action="store_true", help="skip the tau = 0 comparison loop")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sample-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "sm_max_mhz": d.get("sm_max_mhz", 2070.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Work accounting (tile granularity, as the paper counts executed slots).
+# ---------------------------------------------------------------------------
+
+def prefill_units(cfg):
+    t = -(-cfg.L // cfg.block)
+    legal = cfg.B * cfg.H * t * (t + 1) // 2
+    return {"legal_tiles": legal, "tile_flops": 2.0 * cfg.block * cfg.block * cfg.d}
+
+
+def fwd_flops(cfg, kept):
+    u = prefill_units(cfg)
+    return u["tile_flops"] * (u["legal_tiles"] + kept)          # QK on every legal tile, PV on kept
+
+
+def bwd_flops(cfg, kept):
+    u = prefill_units(cfg)
+    return u["tile_flops"] * (u["legal_tiles"] + 4 * kept)      # QK recompute + dP, dV, dK, dQ on kept
+
+
+def decode_bytes(cfg, kept_tiles):
+    tile = cfg.block * cfg.d * 2
+    n_tiles = cfg.B * cfg.Hkv * -(-cfg.N // cfg.block)
+    k_bytes = n_tiles * tile
+    v_bytes = kept_tiles * tile
+    other = cfg.B * cfg.H * cfg.d * 2 * 2 + cfg.num_splits * cfg.B * cfg.H * (cfg.d + 2) * 4 * 2
+    return k_bytes + v_bytes + other
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region.
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mala_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            if self.uuid and self.uuid not in f[1]:
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(sm)
+        loaded = [x for x in sm if x >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the cpu_baseline leg and the reference arm).
+# ---------------------------------------------------------------------------
+
+def _oracle_unit(task):
+    """Runs in a spawned worker with single-threaded BLAS; returns seconds."""
+    import numpy as np  # noqa: F401
+    import oracle as orc
+    from mass_adaptive_sparse_gb300 import synthetic
+    import dataclasses
+    kind, name, seed, arg = task
+    cfg = synthetic.CONFIGS[name]
+    if kind == "prefill":
+        # one head of the same recipe (the sample's unit of work is a tile)
+        cfg = dataclasses.replace(cfg, H=1, Hkv=1, amplitude=cfg.amplitude[:1])
+        x = _WORKER_DATA.get((name, seed))
+        if x is None:
+            x = synthetic.prefill_inputs(cfg, seed=seed)
+            x = {n: x[n][0, :, 0].double().numpy() for n in ("q", "k", "v", "do")}
+            _WORKER_DATA.clear()
+            _WORKER_DATA[(name, seed)] = x
+        t0 = time.perf_counter()
+        scale = 1 / math.sqrt(cfg.d)
+        i = arg
+        f = orc.mala_forward(x["q"], x["k"], x["v"], scale, 1.0, cfg.block, cfg.block, query_blocks=[i])
+        orc.mala_backward(x["q"], x["k"], x["v"], f.o, x["do"], f.lse, scale, 1.0, cfg.block, cfg.block,
+                          tiles=lambda ii, jj: ii == i)
+        return time.perf_counter() - t0, i + 1          # seconds, tiles (fwd) == tiles (bwd)
+    # one (sequence, KV head) group of the same recipe
+    grp = cfg.H // cfg.Hkv
+    cfg = dataclasses.replace(cfg, B=1, H=grp, Hkv=1)
+    x = _WORKER_DATA.get((name, seed + arg))
+    if x is None:
+        y = synthetic.decode_inputs(cfg, seed=seed + arg)
+        x = {n: y[n][0].double().numpy() for n in ("q", "k", "v")}
+        _WORKER_DATA.clear()
+        _WORKER_DATA[(name, seed + arg)] = x
+    t0 = time.perf_counter()
+    orc.mala_decode(x["q"], x["k"][:, 0], x["v"][:, 0], 1 / math.sqrt(cfg.d), 1.0, cfg.block, cfg.num_splits)
+    return time.perf_counter() - t0, 1
+
+
+_WORKER_DATA = {}
+
+
+def _worker_init():
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+
+
+def oracle_sample(workload, pool, cores, rank_seed=0):
+    """Times the oracle on a bounded sample and extrapolates to one full step.
+    Sample: forward + the matching backward dQ column for `cores` query blocks
+    of head 0 of the prefill workload (spread over the sequence), and `cores`
+    (sequence 0, KV head) groups of the decode workload."""
+    from mass_adaptive_sparse_gb300 import synthetic
+    pname, dname = WORKLOADS[workload]
+    pc, dc = synthetic.CONFIGS[pname], synthetic.CONFIGS[dname]
+    tr = pc.L // pc.block
+    nblk = max(2, cores)
+    blocks = [int(round((tr - 1) * (s + 1) / nblk)) for s in range(nblk)]
+    groups = [g % dc.Hkv for g in range(max(1, min(cores, dc.Hkv)))]
+    tasks = [("prefill", pname, pc.seed + rank_seed, i) for i in blocks]
+    tasks += [("decode", dname, dc.seed + rank_seed, g) for g in groups]
+    t0 = time.perf_counter()
+    res = pool.map(_oracle_unit, tasks)
+    wall = time.perf_counter() - t0
+    pre = res[:len(blocks)]
+    dec = res[len(blocks):]
+    pre_cpu = sum(r[0] for r in pre)
+    pre_tiles = sum(r[1] for r in pre)
+    dec_cpu = sum(r[0] for r in dec)
+    full_tiles = prefill_units(pc)["legal_tiles"]
+    full_groups = dc.B * dc.Hkv
+    # per-unit CPU seconds x full units, spread over `cores` workers
+    step_s = (pre_cpu / pre_tiles * full_tiles + dec_cpu / len(dec) * full_groups) / cores
+    sample = (f"fp64 oracle: forward + backward dQ column of query blocks {blocks} (head 0, "
+              f"{pre_tiles} tiles each way) of {pname} and decode of {len(dec)} (sequence 0, KV head) "
+              f"groups of {dname}; extrapolated by tiles ({full_tiles}) and groups ({full_groups})")
+    return step_s * 1e3, wall, sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = min(16, os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_worker_init) as pool:
+        vals = []
+        for s in range(args.warmup + args.steps):
+            v, _, sample = oracle_sample(args.workload, pool, cores)
+            if s >= args.warmup:
+                vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload][0] + "+" + WORKLOADS[args.workload][1],
+                       "tau": 1.0},
+            "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+# ---------------------------------------------------------------------------
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pool = None
+    cores = min(16, os.cpu_count() or 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = mp.get_context("spawn").Pool(cores, initializer=_worker_init)   # before any GPU work
+
+    import torch
+    from mass_adaptive_sparse_gb300 import api, synthetic
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pname, dname = WORKLOADS[args.workload]
+    pc, dc = synthetic.CONFIGS[pname], synthetic.CONFIGS[dname]
+    tau = args.tau
+
+    # inputs (seeded per rank: each rank runs its own replica of the workload)
+    xp = synthetic.prefill_inputs(pc, seed=pc.seed + rank)
+    xd = synthetic.decode_inputs(dc, seed=dc.seed + rank)
+    host_in = {n: xp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_in.update({"qd": xd["q"].pin_memory(), "kc": xd["k"].pin_memory(), "vc": xd["v"].pin_memory()})
+    d = {n: t.to(dev) for n, t in host_in.items()}
+    B, L, H, D = d["q"].shape
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    for n, like in (("dq", "q"), ("dk", "k"), ("dv", "v")):
+        d[n] = torch.empty(d[like].shape, dtype=torch.float32, device=dev)
+    d["ws_b"] = torch.empty(max(256, api.mala_bwd_workspace_size(d["q"], d["k"], torch.float32)),
+                            dtype=torch.uint8, device=dev)
+    d["od"] = torch.empty_like(d["qd"])
+    d["lsed"] = torch.empty((dc.B, dc.H), dtype=torch.float32, device=dev)
+    d["ws_d"] = torch.empty(max(256, api.mala_decode_workspace_size(dc.B, dc.H, dc.d, dc.num_splits)),
+                            dtype=torch.uint8, device=dev)
+    tr = -(-L // pc.block)
+    cf = torch.zeros((B, H, tr), dtype=torch.int32, device=dev)
+    cb = torch.zeros((B, H, tr), dtype=torch.int32, device=dev)
+    cd = torch.zeros((dc.B, dc.Hkv, dc.num_splits), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd(t):
+        api.mala_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], block=pc.block, tau=t, retained_counts=cf)
+
+    def bwd(t):
+        api.mala_bwd(d["q"], d["k"], d["v"], d["o"], d["do"], d["lse"], d["dq"], d["dk"], d["dv"], d["ws_b"],
+                     block=pc.block, tau=t, retained_counts=cb)
+
+    def dec(t):
+        api.mala_decode(d["qd"], d["kc"], d["vc"], d["od"], d["lsed"], d["ws_d"], block=dc.block,
+                        num_splits=dc.num_splits, tau=t, retained_counts=cd)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    def timed(t, steps):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for s in range(steps):
+            ev[s][0].record(stream)
+            fwd(t)
+            ev[s][1].record(stream)
+            bwd(t)
+            ev[s][2].record(stream)
+            dec(t)
+            ev[s][3].record(stream)
+        barrier()
+        ph = {"fwd": [], "bwd": [], "decode": [], "step": []}
+        for e in ev:
+            ph["fwd"].append(e[0].elapsed_time(e[1]))
+            ph["bwd"].append(e[1].elapsed_time(e[2]))
+            ph["decode"].append(e[2].elapsed_time(e[3]))
+            ph["step"].append(e[0].elapsed_time(e[3]))
+        return {k: statistics.mean(v) for k, v in ph.items()}
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # --- tau = 1 (the measured configuration) ---
+    for _ in range(args.warmup):
+        fwd(tau); bwd(tau); dec(tau)
+    barrier()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    n0 = api.mala_launch_count()
+    t_main = timed(tau, args.steps)
+    launches = api.mala_launch_count() - n0
+    clocks = sampler.stop()
+    kept_f = int(cf.sum().item())
+    kept_b = int(cb.sum().item())
+    kept_d = int(cd.sum().item())
+    step_ms = max_over_ranks(t_main["step"])
+
+    # --- tau = 0: dense through the same kernels ---
+    t_dense = None
+    if not args.no_dense:
+        for _ in range(min(args.warmup, 2)):
+            fwd(0.0); bwd(0.0); dec(0.0)
+        barrier()
+        t_dense = timed(0.0, args.steps)
+
+    # --- end to end through the public API with host buffers ---
+    e2e = None
+    if not args.no_e2e:
+        host_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True)
+                    for n in ("o", "lse", "dq", "dk", "dv", "od", "lsed")}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n, t in host_in.items():
+                d[n].copy_(t, non_blocking=True)
+            fwd(tau); bwd(tau); dec(tau)
+            for n, t in host_out.items():
+                t.copy_(d[n], non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
+        e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    ff, fb = fwd_flops(pc, kept_f), bwd_flops(pc, kept_b)
+    db = decode_bytes(dc, kept_d)
+    phases = {
+        "fwd": {"ms": t_main["fwd"], "tflops": ff / t_main["fwd"] / 1e9, "algorithmic_flops": ff,
+                "kept_tiles": kept_f, "legal_tiles": prefill_units(pc)["legal_tiles"]},
+        "bwd": {"ms": t_main["bwd"], "tflops": fb / t_main["bwd"] / 1e9, "algorithmic_flops": fb,
+                "kept_tiles": kept_b, "legal_tiles": prefill_units(pc)["legal_tiles"]},
+        "decode": {"us_per_token": t_main["decode"] * 1e3, "gbs": db / t_main["decode"] / 1e6,
+                   "algorithmic_bytes": db, "kept_tiles": kept_d,
+                   "tiles": dc.B * dc.Hkv * -(-dc.N // dc.block)},
+    }
+    for ph in ("fwd", "bwd"):
+        legal = phases[ph]["legal_tiles"]
+        phases[ph]["slots_per_query"] = phases[ph]["kept_tiles"] * pc.block / (pc.B * pc.H * L)
+        phases[ph]["kept_fraction"] = phases[ph]["kept_tiles"] / legal
+    if t_dense is not None:
+        pd = prefill_units(pc)["legal_tiles"]
+        phases["dense"] = {
+            "fwd_ms": t_dense["fwd"], "bwd_ms": t_dense["bwd"], "decode_us": t_dense["decode"] * 1e3,
+            "fwd_tflops": fwd_flops(pc, pd) / t_dense["fwd"] / 1e9,
+            "bwd_tflops": bwd_flops(pc, pd) / t_dense["bwd"] / 1e9,
+            "speedup_fwd": t_dense["fwd"] / t_main["fwd"], "speedup_bwd": t_dense["bwd"] / t_main["bwd"],
+            "speedup_decode": t_dense["decode"] / t_main["decode"], "step_ms": t_dense["step"]}
+
+    # roofline of the dominant kernel: the CUDA-core kernels are bound by fp32 FMA issue
+    dom = max(("fwd", "bwd"), key=lambda p: t_main[p])
+    alu_peak = SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    achieved = phases[dom]["tflops"]
+    roofline = {"kernel": f"mala_{dom}", "bound": "alu", "achieved": achieved, "peak": alu_peak,
+                "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": None,
+                "peak_source": f"fp32 FMA: {SMS} SMs x 128 lanes x 2 flop x {peaks['sm_max_mhz']:.0f} MHz"}
+    decode_roof = {"achieved": phases["decode"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": phases["decode"]["gbs"] / peaks["hbm_gbs"]}
+
+    cpu = None
+    if pool is not None:
+        val, wall, sample = oracle_sample(args.workload, pool, cores)
+        cpu = {"value": val, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample,
+               "sample_wall_s": wall}
+        pool.close()
+
+    line = {
+        "metric": METRIC, "value": step_ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{pname}+{dname}", "prefill": f"B={pc.B} H={pc.H}/{pc.Hkv} L={pc.L} d={pc.d} "
+                   f"tiles {pc.block}x{pc.block}", "decode": f"B={dc.B} H={dc.H}/{dc.Hkv} N={dc.N} d={dc.d} "
+                   f"block {dc.block} splits {dc.num_splits}", "tau": tau, "grad_dtype": "fp32",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+        "decode_roofline": decode_roof, "phases": phases, "peaks": peaks, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * mala.h -- C ABI of libmala.so: MassAlloc Attention (MALA) on GB300 (sm_103a).
+ *
+ * MALA is causal softmax attention that forms every legal Q K^T score tile and
+ * then runs the post-score work of a tile (softmax update, V load, P V; in the
+ * backward pass P, dP, dS, dQ, dK, dV) only when some valid query row of the
+ * tile gives one of its keys a normalised contribution of at least tau / L_q,
+ * where L_q is the number of keys visible to that row.
+ *
+ * Source of every definition below: "MassAlloc Attention: Let Attention
+ * Allocate Its Own Compute" -- §2.1 (scores, L_q, threshold tau/L_q), §2.2
+ * Eq. (1)-(3) (forward test against the running online-softmax state),
+ * Eq. (4) (backward test against the saved log-normaliser), Algorithm 1
+ * (forward), Algorithm 2 (backward), App. A.1 (fused forward, backward and
+ * split-KV decoding); the split merge is the (m, l, u) identity of "Why exact
+ * attention does not need a quadratic matrix", Method/Mechanism.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers, owned by the caller.  The
+ *    library never allocates or frees device memory; scratch space comes in
+ *    through the `workspace` argument of the calls that need it.
+ *  - Layouts are dense, row-major, head dimension fastest:
+ *      prefill  q, o, dout, dq          [batch, seqlen_q, heads_q,  head_dim]
+ *               k, v, dk, dv            [batch, seqlen_k, heads_kv, head_dim]
+ *               lse                     [batch, heads_q, seqlen_q]   (float)
+ *      decode   q, o                    [batch, heads_q, head_dim]
+ *               k_cache, v_cache        [batch, cache_len, heads_kv, head_dim]
+ *               lse                     [batch, heads_q]              (float)
+ *    Query head h reads key/value head h / (heads_q / heads_kv).
+ *  - Pointers must be 16-byte aligned.
+ *  - Scores are s = softmax_scale * (q . k) computed in fp32; lse is the
+ *    natural-log log-sum-exp over the retained keys (m + log l of Algorithm 1).
+ *    Gradients are with respect to the unscaled q, k and v.
+ *  - tau >= 0.  tau == 0 runs no test at all and gives dense attention
+ *    through the same kernels (§2.3: tau -> 0 recovers full attention).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are reported synchronously, before any
+ *    launch, and leave all outputs untouched.  A failed launch returns
+ *    MALA_ERR_CUDA.  Kernels that wait on on-chip barriers bound every wait;
+ *    an expired wait is recorded in a device status word that
+ *    mala_device_status() reads.
+ *  - Optional instrumentation outputs may be NULL:
+ *      retained_counts  int32, number of retained tiles per unit of work
+ *      tile_mask        uint8, 1 = tile retained, 0 = tile skipped; the call
+ *                       writes the entry of every legal tile and leaves the
+ *                       others unchanged (zero the buffer first).
+ */
+#ifndef MALA_H_
+#define MALA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MALA_OK = 0,
+  MALA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, tau < 0 or NaN */
+  MALA_ERR_UNSUPPORTED = 2,  /* well-formed but not built: head_dim, tile size, dtype */
+  MALA_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the *_workspace_size() */
+  MALA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  MALA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (device status) */
+} mala_status;
+
+typedef enum {
+  MALA_BF16 = 0,
+  MALA_FP32 = 1
+} mala_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mala_status_string(mala_status status);
+
+/*
+ * MALA forward pass (Algorithm 1; test of Eq. (3)).
+ *
+ * For every query block of block_q rows, legal key blocks are visited from the
+ * diagonal toward earlier keys; each tile's scores are formed, and the tile is
+ * skipped iff  rowmax(S) - m - log(l) < log(tau / L_q)  for every valid row
+ * with a legal key in the tile (a row with l = 0 retains).  Skipped tiles load
+ * no V and leave (m, l, O) unchanged.  Writes o = O / l and lse = m + log l.
+ *
+ *  q [batch, seqlen_q, heads_q, head_dim]      in_dtype
+ *  k, v [batch, seqlen_k, heads_kv, head_dim]  in_dtype
+ *  o [batch, seqlen_q, heads_q, head_dim]      out_dtype
+ *  lse [batch, heads_q, seqlen_q]              float
+ *  causal: 1 = key k visible to query q iff k <= q (requires seqlen_q ==
+ *          seqlen_k), L_q = q + 1;  0 = all keys visible, L_q = seqlen_k.
+ *  block_q == block_k, in {64, 128}.  head_dim in {64, 128}.
+ *  retained_counts: [batch, heads_q, ceil(seqlen_q / block_q)]
+ *  tile_mask:       [batch, heads_q, ceil(seqlen_q / block_q), ceil(seqlen_k / block_k)]
+ *  Needs no workspace.
+ */
+mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                     int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int causal,
+                     int block_q, int block_k, float tau, float softmax_scale,
+                     int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/* Bytes of device workspace mala_bwd needs for these sizes. */
+size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                               int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype);
+
+/*
+ * MALA backward pass (Algorithm 2; test of Eq. (4)).
+ *
+ * Key-major: for each key block, the query blocks with a legal entry are
+ * visited in ascending order; the recomputed tile S_ji is skipped iff
+ * S_ji - lse_i < log(tau / L_i) for every valid causal entry.  Retained tiles
+ * run P = exp(S - lse), dP = V dO^T, dS = P * (dP - rowsum(O * dO)),
+ * dV += P dO, dK += dS Q, dQ += dS^T K.  Skipped tiles load no dO.
+ *
+ *  q, o, dout [batch, seqlen_q, heads_q, head_dim]   in_dtype
+ *  k, v       [batch, seqlen_k, heads_kv, head_dim]  in_dtype
+ *  lse        [batch, heads_q, seqlen_q] float, as written by mala_fwd
+ *  dq         [batch, seqlen_q, heads_q, head_dim]   grad_dtype
+ *  dk, dv     [batch, seqlen_k, heads_kv, head_dim]  grad_dtype
+ *  workspace: >= mala_bwd_workspace_size(...) bytes, 256-byte aligned; its
+ *             contents on entry do not matter.
+ *  retained_counts: [batch, heads_q, ceil(seqlen_k / block_k)]
+ *  tile_mask:       [batch, heads_q, ceil(seqlen_q / block_q), ceil(seqlen_k / block_k)]
+ *  Other arguments as for mala_fwd.
+ */
+mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                     int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype, int causal,
+                     int block_q, int block_k, float tau, float softmax_scale,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/* Bytes of device workspace mala_decode needs for these sizes. */
+size_t mala_decode_workspace_size(int batch, int heads_q, int head_dim, int num_splits);
+
+/*
+ * MALA split-KV decode (App. A.1 "Fused decoding execution"; §2.4).
+ *
+ * One new query per sequence against a cache of cache_len tokens that already
+ * holds the current token, so L = cache_len for every row.  The
+ * T = ceil(cache_len / block_k) key tiles are cut into num_splits contiguous
+ * ranges of ceil(T / num_splits) tiles.  Each split starts from its own empty
+ * (m, l), visits its tiles newest to oldest, scores every tile, and skips a
+ * tile iff rowmax - m - log l < log(tau / cache_len) for all query heads of
+ * the KV-head group (the group is the query block; l = 0 retains).  Retained
+ * tiles load V and run softmax and P V.  The splits' (m, l, u) summaries are
+ * merged exactly: m = max m_s, l = sum e^(m_s - m) l_s, u = sum e^(m_s - m) u_s,
+ * o = u / l, lse = m + log l.
+ *
+ *  q [batch, heads_q, head_dim]                     in_dtype
+ *  k_cache, v_cache [batch, cache_len, heads_kv, head_dim]  in_dtype
+ *  o [batch, heads_q, head_dim]                     out_dtype
+ *  lse [batch, heads_q]                             float
+ *  heads_q / heads_kv in {1, 2, 4, 8}; head_dim in {64, 128}; block_k in {64, 128};
+ *  1 <= num_splits <= 256.
+ *  workspace: >= mala_decode_workspace_size(...) bytes, 256-byte aligned.
+ *  retained_counts: [batch, heads_kv, num_splits]
+ *  tile_mask:       [batch, heads_kv, ceil(cache_len / block_k)]
+ */
+mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                        int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                        int num_splits, float tau, float softmax_scale,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word that the
+ * kernels set when a bounded on-chip wait expires.  *device_code receives the
+ * raw word (0 = no event).  Returns MALA_OK, MALA_ERR_TIMEOUT if the word was
+ * set, or MALA_ERR_CUDA if synchronisation failed.
+ */
+mala_status mala_device_status(void* stream, int* device_code);
+
+/* Number of kernels this library has launched in this process (host counter). */
+uint64_t mala_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MALA_H_ */

@@ -1,0 +1,222 @@
+// C ABI of libmala.so (declarations and contracts in include/mala.h):
+// argument validation, workspace layout, kernel selection, device status word.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/mala.h"
+#include "mala_internal.h"
+
+namespace {
+
+using namespace mala;
+
+// Set by kernels whose bounded waits expire; read and cleared by mala_device_status.
+__device__ int g_device_status = 0;
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+int* status_word() {
+  static int* cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_dtype(int d) { return d == MALA_BF16 || d == MALA_FP32; }
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+mala_status finish(cudaError_t e, int launches) {
+  g_launches.fetch_add(static_cast<uint64_t>(launches), std::memory_order_relaxed);
+  return e == cudaSuccess ? MALA_OK : MALA_ERR_CUDA;
+}
+
+// Common shape checks of the prefill calls.
+mala_status check_prefill(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                          int head_dim, int in_dt, int out_dt, int causal, int block_q,
+                          int block_k, float tau, float scale) {
+  if (batch < 1 || seqlen_q < 1 || seqlen_k < 1 || heads_q < 1 || heads_kv < 1) return MALA_ERR_INVALID_ARG;
+  if (batch > 65535 || heads_q > 65535 || heads_q % heads_kv != 0) return MALA_ERR_INVALID_ARG;
+  if (!ok_dtype(in_dt) || !ok_dtype(out_dt)) return MALA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return MALA_ERR_INVALID_ARG;
+  if (causal == 1 && seqlen_q != seqlen_k) return MALA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MALA_ERR_INVALID_ARG;
+  if (block_q < 1 || block_k < 1) return MALA_ERR_INVALID_ARG;
+  if (head_dim < 1) return MALA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
+  if (block_q != block_k || (block_q != 64 && block_q != 128)) return MALA_ERR_UNSUPPORTED;
+  return MALA_OK;
+}
+
+struct BwdLayout {
+  size_t delta = 0, dq_acc = 0, total = 0;
+};
+
+BwdLayout bwd_layout(int batch, int seqlen_q, int heads_q, int head_dim, int grad_dt) {
+  BwdLayout w;
+  const size_t rows = static_cast<size_t>(batch) * seqlen_q * heads_q;
+  w.delta = 0;
+  size_t off = round256(rows * sizeof(float));
+  w.dq_acc = off;
+  if (grad_dt == MALA_BF16) off += round256(rows * head_dim * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mala_status_string(mala_status status) {
+  switch (status) {
+    case MALA_OK: return "MALA_OK";
+    case MALA_ERR_INVALID_ARG: return "MALA_ERR_INVALID_ARG";
+    case MALA_ERR_UNSUPPORTED: return "MALA_ERR_UNSUPPORTED";
+    case MALA_ERR_WORKSPACE: return "MALA_ERR_WORKSPACE";
+    case MALA_ERR_CUDA: return "MALA_ERR_CUDA";
+    case MALA_ERR_TIMEOUT: return "MALA_ERR_TIMEOUT";
+  }
+  return "MALA_ERR_UNKNOWN";
+}
+
+mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                     int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int causal,
+                     int block_q, int block_k, float tau, float softmax_scale,
+                     int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  if (!q || !k || !v || !o || !lse) return MALA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return MALA_ERR_INVALID_ARG;
+  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
+                                 out_dtype, causal, block_q, block_k, tau, softmax_scale);
+  if (st != MALA_OK) return st;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.in_dt = in_dtype; a.out_dt = out_dtype; a.causal = causal; a.blk = block_q;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = launch_fwd_simt(a, s, &launches);
+  return finish(e, launches);
+}
+
+size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                               int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype) {
+  (void)seqlen_k; (void)heads_kv; (void)in_dtype;
+  if (batch < 1 || seqlen_q < 1 || heads_q < 1 || head_dim < 1) return 0;
+  return bwd_layout(batch, seqlen_q, heads_q, head_dim, grad_dtype).total;
+}
+
+mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                     int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype, int causal,
+                     int block_q, int block_k, float tau, float softmax_scale,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
+  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
+                                 grad_dtype, causal, block_q, block_k, tau, softmax_scale);
+  if (st != MALA_OK) return st;
+  if (bwd_simt_smem(in_dtype, head_dim, block_q) > 227u * 1024u) return MALA_ERR_UNSUPPORTED;
+  const BwdLayout w = bwd_layout(batch, seqlen_q, heads_q, head_dim, grad_dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return MALA_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
+  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.in_dt = in_dtype; a.grad_dt = grad_dtype; a.causal = causal; a.blk = block_q;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e; a.scale = softmax_scale;
+  a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.dq_acc = grad_dtype == MALA_FP32 ? static_cast<float*>(dq) : reinterpret_cast<float*>(ws + w.dq_acc);
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = launch_bwd_preprocess(a, s, &launches);
+  if (e == cudaSuccess) e = launch_bwd_simt(a, s, &launches);
+  if (e == cudaSuccess && grad_dtype == MALA_BF16) e = launch_dq_convert(a, s, &launches);
+  return finish(e, launches);
+}
+
+size_t mala_decode_workspace_size(int batch, int heads_q, int head_dim, int num_splits) {
+  if (batch < 1 || heads_q < 1 || head_dim < 1 || num_splits < 1) return 0;
+  return round256(static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 2) * sizeof(float));
+}
+
+mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                        int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                        int num_splits, float tau, float softmax_scale,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  const void* ptrs[] = {q, k_cache, v_cache, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
+  if (batch < 1 || cache_len < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv != 0)
+    return MALA_ERR_INVALID_ARG;
+  if (batch > 65535 || heads_kv > 65535) return MALA_ERR_INVALID_ARG;
+  if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return MALA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MALA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 256 || block_k < 1 || head_dim < 1) return MALA_ERR_INVALID_ARG;
+  const int g = heads_q / heads_kv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
+  if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
+  const size_t need = mala_decode_workspace_size(batch, heads_q, head_dim, num_splits);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return MALA_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  DecArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
+  a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.in_dt = in_dtype; a.out_dt = out_dtype; a.blk = block_k; a.splits = num_splits;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.partial = static_cast<float*>(workspace);
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = launch_decode_simt(a, s, &launches);
+  if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
+  return finish(e, launches);
+}
+
+mala_status mala_device_status(void* stream, int* device_code) {
+  if (!device_code) return MALA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MALA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof(int)) != cudaSuccess) return MALA_ERR_CUDA;
+  const int zero = 0;
+  if (word != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MALA_ERR_CUDA;
+  *device_code = word;
+  return word == 0 ? MALA_OK : MALA_ERR_TIMEOUT;
+}
+
+uint64_t mala_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal declarations shared by the translation units of libmala.so.
+// Host-side argument blocks and the launch functions of every kernel family.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mala {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Element types of the ABI (values match mala_dtype).
+enum Dtype : int { kBF16 = 0, kFP32 = 1 };
+
+// Device status word codes (bitwise OR of events).
+enum StatusCode : int {
+  kStatusWaitTimeout = 1,   // an mbarrier / flag wait hit its iteration cap
+  kStatusBadLaunch = 2      // a kernel found its launch shape inconsistent
+};
+
+struct FwdArgs {
+  const void* q; const void* k; const void* v; void* o; float* lse;
+  int B, Lq, Lk, Hq, Hkv, D;
+  int in_dt, out_dt, causal, blk;
+  float tau;            // >= 0; 0 = dense
+  float log2_tau;       // log2(tau), used only when tau > 0
+  float scale_log2;     // softmax_scale * log2(e): scores kept in log2 units
+  int32_t* counts;      // [B, Hq, Tr] or null
+  uint8_t* mask;        // [B, Hq, Tr, Tc] or null
+  int* status;          // device status word
+};
+
+struct BwdArgs {
+  const void* q; const void* k; const void* v; const void* o; const void* dout;
+  const float* lse; void* dq; void* dk; void* dv;
+  int B, Lq, Lk, Hq, Hkv, D;
+  int in_dt, grad_dt, causal, blk;
+  float tau, log2_tau, scale_log2, scale;
+  float* delta;         // workspace: D_i = rowsum(O * dO)   [B, Hq, Lq]
+  float* dq_acc;        // workspace (or dq itself when fp32): fp32 [B, Lq, Hq, D]
+  void* scratch;        // workspace: kernel-specific staging (may be null)
+  int32_t* counts;      // [B, Hq, Tc] or null
+  uint8_t* mask;        // [B, Hq, Tr, Tc] or null
+  int* status;
+};
+
+struct DecArgs {
+  const void* q; const void* k; const void* v; void* o; float* lse;
+  int B, N, Hq, Hkv, D;
+  int in_dt, out_dt, blk, splits;
+  float tau, log2_tau, scale_log2;
+  float* partial;       // workspace: [splits, B, Hq, D + 2] = (m, l, u[D]) in log2 units
+  int32_t* counts;      // [B, Hkv, splits] or null
+  uint8_t* mask;        // [B, Hkv, T] or null
+  int* status;
+};
+
+// Each launcher returns the first CUDA error and adds its launches to *launches.
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_decode_simt(const DecArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t s, int* launches);
+
+// Shared-memory bytes the SIMT kernels need (0 = shape not supported).
+size_t fwd_simt_smem(int in_dt, int D, int blk);
+size_t bwd_simt_smem(int in_dt, int D, int blk);
+
+}  // namespace mala

@@ -1,0 +1,89 @@
+"""GPU parity of mala_decode (split-KV decode + exact merge) against the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from mass_adaptive_sparse_gb300 import api, synthetic
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None):
+    x = synthetic.decode_inputs(cfg, N=N, B=B, seed=seed)
+    q, k, v = x["q"], x["k"], x["v"]
+    if d is not None:
+        q, k, v = q[..., :d].contiguous(), k[..., :d].contiguous(), v[..., :d].contiguous()
+    if dtype is not None:
+        q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
+    D = q.shape[-1]
+    scale = 1 / math.sqrt(D)
+    o, lse, info = api.decode(q.cuda(), k.cuda(), v.cuda(), tau, block=block, num_splits=splits,
+                              counts=True, mask=True)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 0
+    batches = list(range(B)) if batches is None else batches
+    q64, k64, v64 = (parity.to64(t) for t in (q, k, v))
+    ref = orc.mala_decode_bhd(q64, k64, v64, scale, tau, block, splits, batches=batches)
+    go, glse, gmask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
+    Hq, Hkv = q.shape[1], k.shape[2]
+    grp = Hq // Hkv
+    T = -(-N // block)
+    per = -(-T // splits)
+    fp32 = q.dtype == torch.float32
+    ok = np.zeros((B, Hq), bool)
+    flipped = 0
+    for b in batches:
+        for hk in range(Hkv):
+            diff = gmask[b, hk].astype(bool) != ref["retained"][b, hk]
+            hs = slice(hk * grp, (hk + 1) * grp)
+            if not diff.any():
+                ok[b, hs] = True
+                continue
+            # the first disagreement inside each split (newest tile first) must be borderline
+            for sp in range(splits):
+                idx = [j for j in range(min(T, (sp + 1) * per) - 1, sp * per - 1, -1) if diff[j]]
+                if idx:
+                    assert parity.is_borderline(ref["margin"][b, hk, idx[0]])
+            flipped += 1
+            keep = gmask[b, hk].astype(bool)[None, :]
+            o_r, lse_r = orc.restricted_attention(q64[b, hs], k64[b, :, hk], v64[b, :, hk], scale, keep,
+                                                  grp, block, causal=False)
+            parity.check_close("o (flipped)", go[b, hs], o_r, q.dtype, fp32=fp32)
+    assert flipped <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * Hkv)
+    m = parity.check_close("o", go[ok], ref["o"][ok], q.dtype, fp32=fp32)
+    assert np.abs(glse[ok] - ref["lse"][ok]).max() <= parity.LSE_ABS
+    counts = info["counts"].cpu().numpy()
+    for sp in range(splits):
+        np.testing.assert_array_equal(counts[:, :, sp], gmask[:, :, sp * per:min(T, (sp + 1) * per)].sum(-1))
+    return m, gmask
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+@pytest.mark.parametrize("tau", [0.0, 1.0, 16.0])
+def test_decode_small_bf16(splits, tau):
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 1000, 2, tau, splits, 128, 11)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_decode_small_fp32_d64(block):
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 777, 2, 1.0, 5, block, 12, dtype=torch.float32, d=64)
+
+
+def test_decode_tau0_is_dense_for_any_split():
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _, mask = _check(cfg, 2048, 1, 0.0, 7, 128, 13)
+    assert mask.all()
+
+
+def test_decode_128k_full_size_sampled():
+    """Batch 8, 32 query heads over 8 KV heads, 131072-token cache, 16 splits;
+    sequences 0 and 5 are compared with the oracle."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    for tau in (1.0, 0.0):
+        _check(cfg, cfg.N, cfg.B, tau, cfg.num_splits, cfg.block, cfg.seed, batches=[0, 5])

@@ -1,0 +1,173 @@
+"""GPU parity of mala_fwd / mala_bwd against the fp64 oracle, through the C ABI.
+
+Small cases are compared element by element (several tiles, ragged tails,
+GQA, tau in {0, 1, 4, 1e30}); the 8K, 32K and 128K workloads run at full size
+in the launch configuration the benchmark times and are compared on sampled
+heads and query / key blocks, which the oracle computes exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from mass_adaptive_sparse_gb300 import api, synthetic
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _inputs(cfg, L=None, seed=None, heads=None, hkv=None):
+    x = synthetic.prefill_inputs(cfg, L=L, seed=seed)
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    if heads is not None:
+        q, do = q[:, :, :heads].contiguous(), do[:, :, :heads].contiguous()
+        k, v = k[:, :, :hkv].contiguous(), v[:, :, :hkv].contiguous()
+    return q, k, v, do
+
+
+def _gpu(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def _oracle_bwd_inputs(ref_fwd, gpu_o, gpu_lse, heads, blocks, block, dtype):
+    """Backward inputs: oracle O (rounded to the GPU dtype) and lse (fp32) on
+    the sampled (head, query block) rows, the GPU's own forward elsewhere."""
+    o_in = gpu_o.clone()
+    lse_in = gpu_lse.clone()
+    L = gpu_o.shape[1]
+    for h in heads:
+        for i in blocks:
+            r0, r1 = i * block, min(L, (i + 1) * block)
+            o_in[:, r0:r1, h] = torch.from_numpy(ref_fwd["o"][:, r0:r1, h]).to(dtype).to(DEV)
+            lse_in[:, h, r0:r1] = torch.from_numpy(ref_fwd["lse"][:, h, r0:r1]).float().to(DEV)
+    return o_in, lse_in
+
+
+def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, grad=True,
+              q_blocks=None, dq_blocks=None, dk_blocks=None, ref_heads=None):
+    block = block or cfg.block
+    q, k, v, do = _inputs(cfg, L=L, seed=seed, heads=heads, hkv=hkv)
+    fp32 = (q.dtype == torch.float32) if fp32 is None else fp32
+    d = q.shape[3]
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd, dod = _gpu(q, k, v, do)
+    o, lse, info = api.forward(qd, kd, vd, tau, block=block, counts=True, mask=True)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 0
+    q64, k64, v64, do64 = (parity.to64(t) for t in (q, k, v, do))
+    H = q.shape[2]
+    ref_heads = list(range(H)) if ref_heads is None else ref_heads
+    tr = -(-L // block)
+    fwd_blocks = q_blocks if q_blocks is not None else list(range(tr))
+    if dq_blocks is not None:
+        fwd_blocks = sorted(set(fwd_blocks) | set(dq_blocks) | {i for i in range(tr) if i >= min(dk_blocks)})
+    ref = orc.mala_forward_bshd(q64, k64, v64, scale, tau, block, block, heads=ref_heads,
+                                query_blocks=fwd_blocks)
+    gpu_o, gpu_lse, gpu_mask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
+    metrics = parity.check_forward(gpu_o, gpu_lse, gpu_mask, ref, q64, k64, v64, scale, block, q.dtype,
+                                   fp32, heads=ref_heads, blocks=q_blocks)
+    counts = info["counts"].cpu().numpy()
+    legal_gpu = np.tril(np.ones((tr, tr), bool))
+    np.testing.assert_array_equal(counts, (gpu_mask.astype(bool) & legal_gpu).sum(-1))
+    if not grad:
+        return metrics
+    if dq_blocks is None:
+        o_in, lse_in = _oracle_bwd_inputs(ref, o, lse, ref_heads, range(tr), block, q.dtype)
+        tiles = None
+    else:
+        o_in, lse_in = _oracle_bwd_inputs(ref, o, lse, ref_heads, fwd_blocks, block, q.dtype)
+        tiles = lambda i, j: i in dq_blocks or j in dk_blocks
+    dq, dk, dv, binfo = api.backward(qd, kd, vd, o_in, dod, lse_in, tau, block=block, counts=True, mask=True)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 0
+    o_in64, lse_in64 = parity.to64(o_in), parity.to64(lse_in)
+    refb = orc.mala_backward_bshd(q64, k64, v64, o_in64, do64, lse_in64, scale, tau, block, block,
+                                  heads=ref_heads, tiles=tiles)
+    gpu_b = {"dq": parity.to64(dq), "dk": parity.to64(dk), "dv": parity.to64(dv),
+             "mask": binfo["mask"].cpu().numpy()}
+    # compare only the sampled heads (and KV heads whose every query head is sampled)
+    grp = H // k.shape[2]
+    full_kv = [hk for hk in range(k.shape[2]) if all(h in ref_heads for h in range(hk * grp, (hk + 1) * grp))]
+    dq_rows = np.zeros(q.shape[:3], bool)
+    dk_rows = np.zeros(k.shape[:3], bool)
+    for h in ref_heads:
+        if dq_blocks is None:
+            dq_rows[:, :, h] = True
+        else:
+            for i in dq_blocks:
+                dq_rows[:, i * block:(i + 1) * block, h] = True
+    for hk in full_kv:
+        if dk_blocks is None:
+            dk_rows[:, :, hk] = True
+        else:
+            for j in dk_blocks:
+                dk_rows[:, j * block:(j + 1) * block, hk] = True
+    sel_legal = refb["legal"].copy()
+    gmask = gpu_b["mask"].copy()
+    for h in range(H):
+        if h not in ref_heads:
+            sel_legal[:, h] = False
+    refb_cmp = dict(refb, legal=sel_legal)
+    bm = parity.check_backward(gpu_b, refb_cmp, block, fp32, dq_rows=dq_rows, dk_rows=dk_rows)
+    # backward support is nested in the forward support on oracle-fed rows (MALA §2.2)
+    assert not (refb["retained"] & ~ref["retained"] & sel_legal).any()
+    tc = -(-k.shape[1] // block)
+    np.testing.assert_array_equal(binfo["counts"].cpu().numpy(), (gmask.astype(bool) & legal_gpu[:, :tc]).sum(-2))
+    metrics["bwd"] = bm
+    return metrics
+
+
+def test_tiny_fp32_workload():
+    """B=1, H=2, L=256, d=64, 64x64 tiles, tau=1, fp32: the full case."""
+    cfg = synthetic.CONFIGS["tiny_fp32"]
+    m = _run_case(cfg, cfg.L, 1.0, cfg.seed)
+    assert m["max_abs"] <= parity.FP32_MAX_ABS
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 64.0, 1e30])
+@pytest.mark.parametrize("L", [256, 200])
+def test_tiny_fp32_tau_and_ragged(tau, L):
+    cfg = synthetic.CONFIGS["tiny_fp32"]
+    _run_case(cfg, L, tau, cfg.seed + 7)
+
+
+@pytest.mark.parametrize("block", [64, 128])
+@pytest.mark.parametrize("L,tau", [(1000, 1.0), (777, 4.0), (1024, 0.0), (640, 1e30)])
+def test_bf16_small_cases(block, L, tau):
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run_case(cfg, L, tau, 17, heads=2, hkv=2, block=block)
+
+
+def test_bf16_gqa_small():
+    cfg = synthetic.PrefillConfig("gqa", 1, 4, 2, 600, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.01)
+    _run_case(cfg, 600, 1.0, 23, block=128)
+
+
+def test_fp32_d128_block64():
+    cfg = synthetic.PrefillConfig("f32d128", 1, 2, 2, 300, 128, 64, torch.float32, 3, (4.0,), 3.0, 0.05)
+    _run_case(cfg, 300, 1.0, 29, block=64)
+
+
+def test_prefill_8k_full_size():
+    """All 16 heads run; heads 0 and 9 are compared element by element."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run_case(cfg, cfg.L, 1.0, cfg.seed, ref_heads=[0, 9])
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.0])
+def test_prefill_32k_sampled(tau):
+    cfg = synthetic.CONFIGS["prefill_32k"]
+    tr = cfg.L // cfg.block
+    _run_case(cfg, cfg.L, tau, cfg.seed, ref_heads=[1, 6], q_blocks=[0, 1, tr // 2, tr - 1],
+              dq_blocks=[0, 2], dk_blocks=[tr - 2, tr - 1])
+
+
+def test_prefill_128k_sampled():
+    cfg = synthetic.CONFIGS["prefill_128k"]
+    tr = cfg.L // cfg.block
+    _run_case(cfg, cfg.L, 1.0, cfg.seed, ref_heads=[4], q_blocks=[0, 1, tr - 1],
+              dq_blocks=[1], dk_blocks=[tr - 1])
