@@ -419,7 +419,8 @@ def main():
     }
     for ph in ("fwd", "bwd"):
         legal = phases[ph]["legal_tiles"]
-        phases[ph]["slots_per_query"] = phases[ph]["kept_tiles"] * pc.block / (pc.B * pc.H * L)
+        # Eq. 11: a kept B_q x B_k tile gives B_k post-score slots to each of its B_q rows
+        phases[ph]["slots_per_query"] = phases[ph]["kept_tiles"] * pc.block * pc.block / (pc.B * pc.H * L)
         phases[ph]["kept_fraction"] = phases[ph]["kept_tiles"] / legal
     if t_dense is not None:
         pd = prefill_units(pc)["legal_tiles"]
