@@ -165,6 +165,40 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
                         int32_t* retained_counts, uint8_t* tile_mask, void* stream);
 
 /*
+ * mala_decode without a workspace argument, for callers that cannot allocate
+ * device memory: for example a serving process whose device memory is all
+ * handed out by a fixed pool at start-up and that may not call cudaMalloc
+ * afterwards, or a host framework that calls this library from a plugin with
+ * no allocator and no way to pass scratch space through its own interface.
+ * The paper has no counterpart; it is the same split-KV decode and merge as
+ * mala_decode (same arguments, same kernels, same results), except that the
+ * per-split (m, l, u) records live in a fixed array inside the library.
+ *
+ *  - The array holds mala_decode_noalloc_max_floats() floats (1 Mi floats,
+ *    4 MiB) on every device that loads the library, until the process exits.
+ *    A call needs num_splits * batch * heads_q * (head_dim + 2) floats; larger
+ *    shapes return MALA_ERR_WORKSPACE before anything is launched.
+ *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *    library routine.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents (every split rewrites its whole record before the merge reads
+ *    it, so nothing needs clearing).  Calls that may overlap on the GPU -- on
+ *    different streams without ordering between them -- race on the array and
+ *    must not be issued; calls on one stream are ordered and safe.
+ */
+mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                                int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                                int num_splits, float tau, float softmax_scale,
+                                int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/* Capacity, in floats, of the array mala_decode_noalloc uses (see above). */
+size_t mala_decode_noalloc_max_floats(void);
+
+/*
  * Synchronise `stream`, then read and clear the device status word that the
  * kernels set when a bounded on-chip wait expires.  *device_code receives the
  * raw word (0 = no event).  Returns MALA_OK, MALA_ERR_TIMEOUT if the word was

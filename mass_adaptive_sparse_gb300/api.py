@@ -23,7 +23,8 @@ MALA_BF16, MALA_FP32 = 0, 1
 STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3: "MALA_ERR_WORKSPACE",
           4: "MALA_ERR_CUDA", 5: "MALA_ERR_TIMEOUT"}
 EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bwd",
-           "mala_decode_workspace_size", "mala_decode", "mala_device_status", "mala_launch_count")
+           "mala_decode_workspace_size", "mala_decode", "mala_decode_noalloc",
+           "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count")
 
 
 class MalaError(RuntimeError):
@@ -56,6 +57,10 @@ def lib() -> ctypes.CDLL:
         L.mala_decode_workspace_size.argtypes = [_i] * 4
         L.mala_decode.restype = _i
         L.mala_decode.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
+        L.mala_decode_noalloc.restype = _i
+        L.mala_decode_noalloc.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _vp, _vp]
+        L.mala_decode_noalloc_max_floats.restype = _sz
+        L.mala_decode_noalloc_max_floats.argtypes = []
         L.mala_device_status.restype = _i
         L.mala_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
         L.mala_launch_count.restype = ctypes.c_uint64
@@ -138,6 +143,18 @@ def mala_decode(q, k_cache, v_cache, o, lse, workspace, *, block=128, num_splits
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, N, Hq, Hkv, D, _dt(q), _dt(o),
         block, num_splits, float(tau), _scale(D, softmax_scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(retained_counts), _ptr(tile_mask),
+        _stream(stream)))
+
+
+def mala_decode_noalloc(q, k_cache, v_cache, o, lse, *, block=128, num_splits=16, tau=1.0,
+                        softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
+    """mala_decode with the split records in the library's fixed device array
+    (for callers that cannot allocate; see include/mala.h)."""
+    B, Hq, D = q.shape
+    N, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _check("mala_decode_noalloc", lib().mala_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, N, Hq, Hkv, D, _dt(q), _dt(o),
+        block, num_splits, float(tau), _scale(D, softmax_scale), _ptr(retained_counts), _ptr(tile_mask),
         _stream(stream)))
 
 

@@ -64,6 +64,26 @@ struct BwdLayout {
   size_t delta = 0, dq_acc = 0, total = 0;
 };
 
+// Scratch of mala_decode_noalloc: the per-split (m, l, u) records, at most
+// kNoAllocDecodeFloats floats (4 MiB).  Every device that loads the library
+// holds one copy until the process exits.
+constexpr size_t kNoAllocDecodeFloats = size_t(1) << 20;
+__device__ __align__(256) float g_decode_scratch[kNoAllocDecodeFloats];
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device (the host-side name is only a stand-in, not a device address).
+float* decode_scratch() {
+  static float* cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<float*>(p);
+  }
+  return cache[dev];
+}
+
 BwdLayout bwd_layout(int batch, int seqlen_q, int heads_q, int head_dim, int grad_dt) {
   BwdLayout w;
   const size_t rows = static_cast<size_t>(batch) * seqlen_q * heads_q;
@@ -205,6 +225,47 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
   if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
   return finish(e, launches);
 }
+
+mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                                int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                                int num_splits, float tau, float softmax_scale,
+                                int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  const void* ptrs[] = {q, k_cache, v_cache, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
+  if (batch < 1 || cache_len < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv != 0)
+    return MALA_ERR_INVALID_ARG;
+  if (batch > 65535 || heads_kv > 65535) return MALA_ERR_INVALID_ARG;
+  if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return MALA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MALA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 256 || block_k < 1 || head_dim < 1) return MALA_ERR_INVALID_ARG;
+  const int g = heads_q / heads_kv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
+  if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 2);
+  if (need > kNoAllocDecodeFloats) return MALA_ERR_WORKSPACE;
+  float* scratch = decode_scratch();
+  int* status = status_word();
+  if (!scratch || !status) return MALA_ERR_CUDA;
+  DecArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
+  a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.in_dt = in_dtype; a.out_dt = out_dtype; a.blk = block_k; a.splits = num_splits;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.partial = scratch;
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = launch_decode_simt(a, s, &launches);
+  if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
+  return finish(e, launches);
+}
+
+size_t mala_decode_noalloc_max_floats(void) { return kNoAllocDecodeFloats; }
 
 mala_status mala_device_status(void* stream, int* device_code) {
   if (!device_code) return MALA_ERR_INVALID_ARG;

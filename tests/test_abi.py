@@ -92,5 +92,17 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
     assert rc == code
 
 
+def test_noalloc_decode_rejects_oversize_before_any_launch(lib):
+    cap = lib.mala_decode_noalloc_max_floats()
+    assert cap == 1 << 20
+    # 16 splits * 64 sequences * 32 heads * 130 floats > cap: rejected by shape alone
+    rc = lib.mala_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 1024, 32, 8, 128, 0, 0, 128, 16, 1.0, 0.08,
+                                 None, None, None)
+    assert rc == 3
+    rc = lib.mala_decode_noalloc(None, FAKE, FAKE, FAKE, FAKE, 1, 1024, 32, 8, 128, 0, 0, 128, 16, 1.0, 0.08,
+                                 None, None, None)
+    assert rc == 1
+
+
 def test_device_status_rejects_null(lib):
     assert lib.mala_device_status(None, None) == 1
