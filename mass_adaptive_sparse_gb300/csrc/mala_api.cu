@@ -133,7 +133,7 @@ mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  cudaError_t e = launch_fwd_simt(a, s, &launches);
+  cudaError_t e = fwd_tc_supported(a) ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
   return finish(e, launches);
 }
 

@@ -65,6 +65,10 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s, int* launche
 cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t s, int* launches);
 
+// Tensor-core (tcgen05) kernels: bf16 inputs, head_dim 128, 128 x 128 tiles.
+bool fwd_tc_supported(const FwdArgs& a);
+cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches);
+
 // Shared-memory bytes the SIMT kernels need (0 = shape not supported).
 size_t fwd_simt_smem(int in_dt, int D, int blk);
 size_t bwd_simt_smem(int in_dt, int D, int blk);

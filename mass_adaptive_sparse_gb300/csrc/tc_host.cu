@@ -1,0 +1,45 @@
+// Host helpers of the tensor-core kernels: TMA tensor-map encoding.
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
+
+namespace mala {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+// [B, L, H, D] tensor of 16-bit elements, D contiguous, viewed as the 4-D
+// array (D, H, L, B).  Box {64, 1, box_rows, 1}: 64 elements = 128 bytes along
+// D (one swizzle row) by box_rows consecutive positions of one head.
+bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int L, int H, int D, int box_rows,
+                     bool fp16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t e = 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(H) * D * e,
+                           static_cast<cuuint64_t>(L) * H * D * e};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mala
