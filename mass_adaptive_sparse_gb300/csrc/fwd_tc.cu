@@ -200,7 +200,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk));
     const bool test = a.tau > 0.f;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m_used = -INFINITY, l = 0.f;
+    // l: exact fp32 sum of P (Eq. 3 test and lse); lr: sum of the bf16-rounded P
+    // that enters the P V product (normalises O consistently with it)
+    float m_used = -INFINITY, l = 0.f, lr = 0.f;
     int nret = 0, vissued = 0;
     bool ok = true;
     uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc : nullptr;
@@ -258,16 +260,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
       const float nscale = a.scale_log2;
-      float rowsum = 0.f;
+      float rowsum = 0.f, rowsum_r = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), nscale, -mref));
         const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), nscale, -mref));
         const uint32_t w = pack_bf16(p0, p1);
-        rowsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        rowsum += p0 + p1;
+        rowsum_r += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         sr[c] = w;                            // P packed over the consumed scores
       }
       l = l * alpha + rowsum;
+      lr = lr * alpha + rowsum_r;
       // O must be rescaled when the reference max moved: wait for the last P V
       if (nret > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const int prev = nret - 1;
@@ -304,7 +308,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     fence_after_sync();
     if (__all_sync(0xffffffffu, ok) && !*abortp) {
       Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
-      const float inv = 1.f / l;
+      const float inv = 1.f / lr;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];
