@@ -1,0 +1,538 @@
+// MALA backward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// "MassAlloc Attention: Let Attention Allocate Its Own Compute", Algorithm 2
+// and §2.2 Eq. (4), key-major (App. A.1): one CTA owns a 128-key block of one
+// KV head and visits, for each query head of the group, the query blocks with
+// a legal entry in ascending order.  Each tile's transposed scores
+// S^T = K Q^T are recomputed; the tile is skipped iff S - lse < log(tau / L_q)
+// on every valid causal entry.  A skipped tile loads no dO and runs no
+// post-score work.  A retained tile runs
+//   P^T = exp(S^T - lse), dP^T = V dO^T, dS^T = P^T o (dP^T - D),
+//   dV += P^T dO, dK += dS^T Q, dQ += dS K  (dQ added to an fp32 accumulator).
+//
+// All post-score products run on fp16 operands (exact fp16 copies of Q, K, V,
+// dO made by the preprocess kernel); P and dS are rounded to fp16, which keeps
+// the gradients within 2e-4 mean relative error where bf16 would not.
+//
+// 192 threads: warps 0-3 = "math" warpgroup (thread r owns key row r = TMEM
+// lane r for S^T, P^T, dP^T, dV, dK, and query row r for the dQ read-out),
+// warp 4 = TMA producer (K, V once; Q ring), warp 5 = MMA issuer.
+// TMEM columns: [0,128) S^T then P^T (fp16 in [0,64)); [128,256) dP^T then
+// dQ; [256,384) dV; [384,512) dK.  dS is written to shared memory once, in the
+// 128-byte-swizzled layout that is K-major for dK = dS^T Q (A = dS^T) and
+// MN-major for dQ = dS K (A = dS).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "mala_internal.h"
+#include "tc_common.cuh"
+
+namespace mala {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 128;
+constexpr int kBlk = 128;
+constexpr int kTile = kBlk * kD * 2;    // 32 KiB of fp16
+constexpr int kHalf = kTile / 2;
+constexpr int kThreads = 192;
+// shared memory: K, V, Q[2], dO, dS
+constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile;
+constexpr int kSmem = 6 * kTile + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t do_full, do_empty;
+  uint64_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free;
+  uint64_t fin;
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))); }
+__device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <typename Tg>
+__device__ __forceinline__ void store_grad_row(Tg* dst, const uint32_t* v, float scale);
+
+template <>
+__device__ __forceinline__ void store_grad_row<float>(float* dst, const uint32_t* v, float scale) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d4[i] = make_float4(__uint_as_float(v[4 * i]) * scale, __uint_as_float(v[4 * i + 1]) * scale,
+                        __uint_as_float(v[4 * i + 2]) * scale, __uint_as_float(v[4 * i + 3]) * scale);
+}
+
+template <>
+__device__ __forceinline__ void store_grad_row<__nv_bfloat16>(__nv_bfloat16* dst, const uint32_t* v, float scale) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w;
+    w.x = pack_bf16(__uint_as_float(v[8 * i + 0]) * scale, __uint_as_float(v[8 * i + 1]) * scale);
+    w.y = pack_bf16(__uint_as_float(v[8 * i + 2]) * scale, __uint_as_float(v[8 * i + 3]) * scale);
+    w.z = pack_bf16(__uint_as_float(v[8 * i + 4]) * scale, __uint_as_float(v[8 * i + 5]) * scale);
+    w.w = pack_bf16(__uint_as_float(v[8 * i + 6]) * scale, __uint_as_float(v[8 * i + 7]) * scale);
+    d4[i] = w;
+  }
+}
+
+template <typename Tg>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+              const BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ uint32_t tmem_sh;
+  __shared__ int flag;
+  __shared__ int abort_flag;
+  __shared__ float vec_lse[2][kBlk], vec_d[2][kBlk], vec_c[2][kBlk];
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO, sDS = base + kOffDS;
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int bh = blockIdx.x;
+  const int hk = bh % a.Hkv, b = bh / a.Hkv;
+  const int kb = blockIdx.y;                                   // small key blocks (most work) first
+  const int G = a.Hq / a.Hkv;
+  const int Tr = (a.Lq + kBlk - 1) / kBlk, Tc = (a.Lk + kBlk - 1) / kBlk;
+  const int ibot = a.causal ? kb : 0;
+  const int ni = Tr - ibot;
+  const int ntiles = G * ni;
+
+  if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_sh));
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bars.kv_full), 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(smem_u32(&bars.q_full[i]), 1); mbar_init(smem_u32(&bars.q_empty[i]), 1); }
+    mbar_init(smem_u32(&bars.do_full), 1);
+    mbar_init(smem_u32(&bars.do_empty), 1);
+    mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.p_ready), 1);
+    mbar_init(smem_u32(&bars.dp_full), 1);
+    mbar_init(smem_u32(&bars.ds_ready), 1);
+    mbar_init(smem_u32(&bars.dq_full), 1);
+    mbar_init(smem_u32(&bars.dq_free), 1);
+    mbar_init(smem_u32(&bars.fin), 1);
+    fence_barrier_init();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tmem_sh;
+  volatile int* abortp = &abort_flag;
+
+  if (warp == 4) {
+    // ---------------- TMA producer: K, V once; Q ring of 2 ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      prefetch_tensormap(&mdo);
+      const uint32_t kvf = smem_u32(&bars.kv_full);
+      mbar_expect_tx(kvf, 2 * kTile);
+      tma_load_4d(sK, &mk, kvf, 0, hk, kb * kBlk, b);
+      tma_load_4d(sK + kHalf, &mk, kvf, 64, hk, kb * kBlk, b);
+      tma_load_4d(sV, &mv, kvf, 0, hk, kb * kBlk, b);
+      tma_load_4d(sV + kHalf, &mv, kvf, 64, hk, kb * kBlk, b);
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t & 1, n = t >> 1;
+        if (n > 0 && !mbar_wait(smem_u32(&bars.q_empty[s]), (n - 1) & 1, abortp, a.status)) break;
+        const int h = hk * G + t / ni, i = ibot + t % ni;
+        const uint32_t qf = smem_u32(&bars.q_full[s]);
+        mbar_expect_tx(qf, kTile);
+        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, i * kBlk, b);
+        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, i * kBlk, b);
+        ++issued;
+      }
+      mbar_wait(kvf, 0, abortp, a.status);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait(smem_u32(&bars.q_full[t & 1]), (t >> 1) & 1, abortp, a.status);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_f16(0, 0, 0, kBlk, kBlk);    // A, B K-major (fp16)
+      constexpr uint32_t id_kmn = idesc_f16(0, 0, 1, kBlk, kD);     // A K-major (or TMEM), B MN-major
+      constexpr uint32_t id_mnmn = idesc_f16(0, 1, 1, kBlk, kD);    // A, B MN-major
+      bool ok = mbar_wait(smem_u32(&bars.kv_full), 0, abortp, a.status);
+      auto issue_qk = [&](int t) -> bool {
+        const int s = t & 1;
+        if (!mbar_wait(smem_u32(&bars.q_full[s]), (t >> 1) & 1, abortp, a.status)) return false;
+        fence_after_sync();
+        const uint32_t qb = sQ + s * kTile;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
+          mma_ss(tmem + kColS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(qb + off), id_kk, k > 0);
+        }
+        mma_commit(smem_u32(&bars.s_full));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      int nret = 0;
+      for (int t = 0; ok && t < ntiles; ++t) {
+        if (!mbar_wait(smem_u32(&bars.p_ready), t & 1, abortp, a.status)) break;
+        fence_after_sync();
+        const int ret = flag;
+        const uint32_t qb = sQ + (t & 1) * kTile;
+        if (ret) {
+          if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status)) break;
+          if (nret > 0 && !mbar_wait(smem_u32(&bars.dq_free), (nret - 1) & 1, abortp, a.status)) break;
+          fence_after_sync();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
+            mma_ss(tmem + kColDP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
+          }
+          mma_commit(smem_u32(&bars.dp_full));
+          // dV += P^T dO   (A = P^T from TMEM)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColDV, tmem + kColS + k * 8, desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn,
+                   (nret > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bars.do_empty));
+        }
+        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
+        if (!ret) {
+          mma_commit(smem_u32(&bars.q_empty[t & 1]));
+          continue;
+        }
+        if (!mbar_wait(smem_u32(&bars.ds_ready), nret & 1, abortp, a.status)) break;
+        fence_after_sync();
+        // dK += dS^T Q   (A = dS^T: K-major view of the dS tile)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + kColDK, desc_kmajor_sw128(sDS + (k / 4) * kHalf + (k % 4) * 32),
+                 desc_mnmajor_sw128(qb + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars.q_empty[t & 1]));
+        // dQ = dS K   (A = dS: MN-major view of the same tile), into the dP columns
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + kColDP, desc_mnmajor_sw128(sDS + k * 2048, kHalf, 1024),
+                 desc_mnmajor_sw128(sK + k * 2048, kHalf, 1024), id_mnmn, k > 0);
+        mma_commit(smem_u32(&bars.dq_full));
+        ++nret;
+      }
+      mma_commit(smem_u32(&bars.fin));
+      mbar_wait(smem_u32(&bars.fin), 0, abortp, a.status);
+    }
+  } else {
+    // ---------------- math warpgroup ----------------
+    const int r = tid;
+    const int key = kb * kBlk + r;
+    const bool key_ok = key < a.Lk;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool test = a.tau > 0.f;
+    const float sl2 = a.scale_log2;
+    const float inv_sl2 = 1.f / sl2;
+    int nret = 0, do_issued = 0, head_kept = 0;
+    bool ok = true;
+    int prev_q0 = 0, prev_h = 0;   // query block / head of the last retained tile (for the dQ read-out)
+
+    // per-query vectors of tile t: lse (log2 units), D, decision threshold in raw dot units
+    float n_lse = 0.f, n_d = 0.f, n_c = 0.f;
+    auto fetch = [&](int t) {
+      const int h = hk * G + t / ni, i = ibot + t % ni;
+      const int q = i * kBlk + r;
+      if (q < a.Lq) {
+        const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.Lq + q;
+        n_lse = a.lse[off] * kLog2e;
+        n_d = a.delta[off];
+        const float thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
+                               : -INFINITY;
+        n_c = (n_lse + thr) * inv_sl2;        // keep iff raw S >= n_c
+      } else {
+        n_lse = 0.f; n_d = 0.f; n_c = INFINITY;
+      }
+    };
+    if (ntiles > 0) fetch(0);
+
+    auto readout_dq = [&](int which) {      // add the finished dQ tile into the fp32 accumulator
+      ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
+      fence_after_sync();
+      if (__all_sync(0xffffffffu, ok)) {
+        const int q = prev_q0 + r;
+        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + (q < a.Lq ? q : 0)) * a.Hq + prev_h) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32_sync(lane_addr + kColDP + c * 32, v);
+          if (q < a.Lq) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4(dst + c * 32 + e, __uint_as_float(v[e]) * a.scale, __uint_as_float(v[e + 1]) * a.scale,
+                         __uint_as_float(v[e + 2]) * a.scale, __uint_as_float(v[e + 3]) * a.scale);
+          }
+        }
+      }
+      fence_before_sync();
+    };
+
+    for (int t = 0; t < ntiles; ++t) {
+      const int h = hk * G + t / ni, i = ibot + t % ni;
+      const int q0 = i * kBlk;
+      const int vb = t & 1;
+      vec_lse[vb][r] = n_lse;
+      vec_d[vb][r] = n_d;
+      vec_c[vb][r] = n_c;
+      named_sync(1, 128);
+      if (t + 1 < ntiles) fetch(t + 1);
+
+      ok = mbar_wait(smem_u32(&bars.s_full), t & 1, abortp, a.status);
+      fence_after_sync();
+      // Eq. (4): keep iff some valid entry has S - lse >= log(tau / L_q).  S^T is
+      // read from TMEM 32 columns at a time (again below for P if retained).
+      const bool diag = a.causal && q0 == kb * kBlk;
+      const int qlim = a.Lq - q0;                 // query columns at or beyond this are out of range
+      const int qmin = diag ? r : 0;              // causal: query >= key inside the diagonal tile
+      int keep_row = 0;
+      if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32_sync(lane_addr + kColS + c * 32, sr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int q = c * 32 + e;
+            keep_row |= (key_ok && q < qlim && q >= qmin && __uint_as_float(sr[e]) >= vec_c[vb][q]) ? 1 : 0;
+          }
+        }
+      }
+      fence_before_sync();
+      const int keep = named_vote_or(1, 128, keep_row);
+      if (named_vote_or(1, 128, !ok || *abortp)) break;
+      uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + i) * Tc + kb : nullptr;
+      if (r == 0) {
+        head_kept += keep;
+        if (t % ni == ni - 1) {                   // last query block of this head
+          if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tc + kb] = head_kept;
+          head_kept = 0;
+        }
+      }
+      if (!keep) {
+        if (r == 0) {
+          if (mrow) *mrow = 0;
+          flag = 0;
+          mbar_arrive(smem_u32(&bars.p_ready));
+        }
+        continue;
+      }
+      if (r == 0) {
+        if (mrow) *mrow = 1;
+        // dO of this tile, loaded only now that the tile is retained
+        if (nret > 0) ok = mbar_wait(smem_u32(&bars.do_empty), (nret - 1) & 1, abortp, a.status);
+        if (ok) {
+          const uint32_t df = smem_u32(&bars.do_full);
+          mbar_expect_tx(df, kTile);
+          tma_load_4d(sDO, &mdo, df, 0, h, q0, b);
+          tma_load_4d(sDO + kHalf, &mdo, df, 64, h, q0, b);
+          ++do_issued;
+        }
+      }
+      // P^T = exp2(S * scale_log2 - lse) in fp16, over S's columns
+      // P^T = exp2(S * scale_log2 - lse) in fp16, written over S's first 64 columns
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32_sync(lane_addr + kColS + c * 32, sr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = c * 32 + 2 * e;
+          const bool l0 = key_ok && q < qlim && q >= qmin;
+          const bool l1 = key_ok && q + 1 < qlim && q + 1 >= qmin;
+          const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[2 * e]), sl2, -vec_lse[vb][q])) : 0.f;
+          const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -vec_lse[vb][q + 1])) : 0.f;
+          pk[c * 16 + e] = pack_f16(p0, p1);
+        }
+      }
+      tmem_st32(lane_addr + kColS, pk);
+      tmem_st32(lane_addr + kColS + 32, pk + 32);
+      tmem_st_wait();
+      fence_before_sync();
+      if (named_vote_or(1, 128, !ok || *abortp)) break;
+      if (r == 0) {
+        flag = 1;
+        mbar_arrive(smem_u32(&bars.p_ready));
+      }
+      // dQ of the previous retained tile leaves the dP columns before dP^T lands there
+      if (nret > 0) {
+        readout_dq(nret - 1);
+        if (named_vote_or(1, 128, !ok || *abortp)) break;
+        if (r == 0) mbar_arrive(smem_u32(&bars.dq_free));
+      }
+      ok = mbar_wait(smem_u32(&bars.dp_full), nret & 1, abortp, a.status);
+      fence_after_sync();
+      // dS^T = P^T o (dP^T - D), fp16, into the swizzled dS tile (row = key r)
+      if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dp[32];
+          tmem_ld32_sync(lane_addr + kColDP + c * 32, dp);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q = c * 32 + 2 * e;
+            const uint32_t pw = pk[c * 16 + e];
+            const float ds0 = f16_lo(pw) * (__uint_as_float(dp[2 * e]) - vec_d[vb][q]);
+            const float ds1 = f16_hi(pw) * (__uint_as_float(dp[2 * e + 1]) - vec_d[vb][q + 1]);
+            w[e] = pack_f16(ds0, ds1);
+          }
+          // queries c*32 .. c*32+31 -> 4 chunks of 8 in the 64-query half (c / 2)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int chunk = (c % 2) * 4 + u;          // 16-byte chunk inside the 128-byte row
+            const uint32_t addr = sDS + (c / 2) * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                         : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      if (named_vote_or(1, 128, !ok || *abortp)) break;
+      if (r == 0) mbar_arrive(smem_u32(&bars.ds_ready));
+      prev_q0 = q0;
+      prev_h = h;
+      ++nret;
+    }
+
+    // last dQ tile, then dK, dV out of TMEM (loads are warp-collective; stores per key)
+    if (nret > 0 && __all_sync(0xffffffffu, ok && !*abortp)) readout_dq(nret - 1);
+    fence_after_sync();
+    if (__all_sync(0xffffffffu, ok && !*abortp)) {
+      const size_t off = ((static_cast<size_t>(b) * a.Lk + (key_ok ? key : 0)) * a.Hkv + hk) * kD;
+      Tg* dvp = static_cast<Tg*>(a.dv) + off;
+      Tg* dkp = static_cast<Tg*>(a.dk) + off;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        if (nret > 0) {
+          tmem_ld32_sync(lane_addr + kColDV + c * 32, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (key_ok) store_grad_row<Tg>(dvp + c * 32, v, 1.f);
+        if (nret > 0) tmem_ld32_sync(lane_addr + kColDK + c * 32, v);
+        if (key_ok) store_grad_row<Tg>(dkp + c * 32, v, a.scale);
+      }
+    }
+    // a dO load issued for an abandoned tile must land before the CTA exits
+    if (r == 0 && *abortp && do_issued > 0)
+      mbar_wait(smem_u32(&bars.do_full), (do_issued - 1) & 1, abortp, a.status);
+    fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    fence_after_sync();
+    tmem_dealloc<512>(tmem);
+  }
+}
+
+// Exact fp16 copies of q, k, v, dO (bf16 in; exact for |x| in the fp16
+// normal range), D = rowsum(O * dO), and a zeroed fp32 dQ accumulator.  One
+// warp per row; each lane converts 4 of the 128 elements.
+__global__ void bwd_tc_prep_kernel(const BwdArgs a, uint32_t* q16, uint32_t* k16, uint32_t* v16, uint32_t* do16) {
+  const size_t qrows = static_cast<size_t>(a.B) * a.Lq * a.Hq;
+  const size_t krows = static_cast<size_t>(a.B) * a.Lk * a.Hkv;
+  const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (row < qrows) {
+    const uint2 qv = reinterpret_cast<const uint2*>(a.q)[row * 32 + lane];
+    const uint2 dv = reinterpret_cast<const uint2*>(a.dout)[row * 32 + lane];
+    const uint2 ov = reinterpret_cast<const uint2*>(a.o)[row * 32 + lane];
+    reinterpret_cast<uint2*>(q16)[row * 32 + lane] =
+        make_uint2(pack_f16(bf16_lo(qv.x), bf16_hi(qv.x)), pack_f16(bf16_lo(qv.y), bf16_hi(qv.y)));
+    reinterpret_cast<uint2*>(do16)[row * 32 + lane] =
+        make_uint2(pack_f16(bf16_lo(dv.x), bf16_hi(dv.x)), pack_f16(bf16_lo(dv.y), bf16_hi(dv.y)));
+    float s = bf16_lo(ov.x) * bf16_lo(dv.x) + bf16_hi(ov.x) * bf16_hi(dv.x) +
+              bf16_lo(ov.y) * bf16_lo(dv.y) + bf16_hi(ov.y) * bf16_hi(dv.y);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    reinterpret_cast<float4*>(a.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      const int h = static_cast<int>(row % a.Hq);
+      const size_t bq = row / a.Hq;
+      const int q = static_cast<int>(bq % a.Lq);
+      const size_t bb = bq / a.Lq;
+      a.delta[(bb * a.Hq + h) * a.Lq + q] = s;
+    }
+  }
+  if (row < krows) {
+    const uint2 kv = reinterpret_cast<const uint2*>(a.k)[row * 32 + lane];
+    const uint2 vv = reinterpret_cast<const uint2*>(a.v)[row * 32 + lane];
+    reinterpret_cast<uint2*>(k16)[row * 32 + lane] =
+        make_uint2(pack_f16(bf16_lo(kv.x), bf16_hi(kv.x)), pack_f16(bf16_lo(kv.y), bf16_hi(kv.y)));
+    reinterpret_cast<uint2*>(v16)[row * 32 + lane] =
+        make_uint2(pack_f16(bf16_lo(vv.x), bf16_hi(vv.x)), pack_f16(bf16_lo(vv.y), bf16_hi(vv.y)));
+  }
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const BwdArgs& a) {
+  return a.in_dt == kBF16 && a.D == kD && a.blk == kBlk;
+}
+
+size_t bwd_tc_scratch_bytes(int B, int Lq, int Lk, int Hq, int Hkv, int D) {
+  return 2 * (static_cast<size_t>(B) * Lq * Hq * D + static_cast<size_t>(B) * Lk * Hkv * D) * sizeof(__half);
+}
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches) {
+  // fp16 copies: q, dO [B, Lq, Hq, D] then k, v [B, Lk, Hkv, D] (two halves per 32-bit word)
+  uint32_t* q16 = static_cast<uint32_t*>(a.scratch);
+  uint32_t* do16 = q16 + static_cast<size_t>(a.B) * a.Lq * a.Hq * kD / 2;
+  uint32_t* k16 = do16 + static_cast<size_t>(a.B) * a.Lq * a.Hq * kD / 2;
+  uint32_t* v16 = k16 + static_cast<size_t>(a.B) * a.Lk * a.Hkv * kD / 2;
+  const size_t rows = std::max(static_cast<size_t>(a.B) * a.Lq * a.Hq, static_cast<size_t>(a.B) * a.Lk * a.Hkv);
+  bwd_tc_prep_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(a, q16, k16, v16, do16);
+  ++*launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bshd_map(&mq, q16, a.B, a.Lq, a.Hq, kD, kBlk, true) ||
+      !encode_bshd_map(&mdo, do16, a.B, a.Lq, a.Hq, kD, kBlk, true) ||
+      !encode_bshd_map(&mk, k16, a.B, a.Lk, a.Hkv, kD, kBlk, true) ||
+      !encode_bshd_map(&mv, v16, a.B, a.Lk, a.Hkv, kD, kBlk, true))
+    return cudaErrorInvalidValue;
+  const int tc = (a.Lk + kBlk - 1) / kBlk;
+  dim3 grid(a.Hkv * a.B, tc);
+  ++*launches;
+  if (a.grad_dt == kBF16) {
+    auto kern = bwd_tc_kernel<__nv_bfloat16>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+  } else {
+    auto kern = bwd_tc_kernel<float>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mala

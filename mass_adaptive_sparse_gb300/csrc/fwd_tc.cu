@@ -212,7 +212,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.s_full[sb]), (t / kNS) & 1, abortp, a.status);
       fence_after_sync();
       uint32_t sr[128];                       // raw scores Q.K (fp32 bits), later packed P
-      if (ok) {
+      if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32_sync(lane_addr + sb * 128 + c * 32, sr + c * 32);
       }
@@ -306,7 +306,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.pv_done[last & 1]), (last >> 1) & 1, abortp, a.status);
     }
     fence_after_sync();
-    if (__all_sync(0xffffffffu, ok) && !*abortp) {
+    if (__all_sync(0xffffffffu, ok && !*abortp)) {
       Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
       const float inv = 1.f / lr;
 #pragma unroll

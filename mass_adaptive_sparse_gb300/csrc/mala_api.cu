@@ -61,7 +61,7 @@ mala_status check_prefill(int batch, int seqlen_q, int seqlen_k, int heads_q, in
 }
 
 struct BwdLayout {
-  size_t delta = 0, dq_acc = 0, total = 0;
+  size_t delta = 0, dq_acc = 0, scratch = 0, total = 0;
 };
 
 // Scratch of mala_decode_noalloc: the per-split (m, l, u) records, at most
@@ -84,13 +84,19 @@ float* decode_scratch() {
   return cache[dev];
 }
 
-BwdLayout bwd_layout(int batch, int seqlen_q, int heads_q, int head_dim, int grad_dt) {
+// Workspace: D [B, Hq, Lq] fp32 | dQ accumulator fp32 (bf16 gradients only) |
+// fp16 operand copies (tensor-core path: bf16 inputs, head_dim 128).
+BwdLayout bwd_layout(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv, int head_dim,
+                     int in_dt, int grad_dt) {
   BwdLayout w;
   const size_t rows = static_cast<size_t>(batch) * seqlen_q * heads_q;
   w.delta = 0;
   size_t off = round256(rows * sizeof(float));
   w.dq_acc = off;
   if (grad_dt == MALA_BF16) off += round256(rows * head_dim * sizeof(float));
+  w.scratch = off;
+  if (in_dt == MALA_BF16 && head_dim == 128)
+    off += round256(bwd_tc_scratch_bytes(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim));
   w.total = off;
   return w;
 }
@@ -139,9 +145,8 @@ mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float
 
 size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
                                int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype) {
-  (void)seqlen_k; (void)heads_kv; (void)in_dtype;
-  if (batch < 1 || seqlen_q < 1 || heads_q < 1 || head_dim < 1) return 0;
-  return bwd_layout(batch, seqlen_q, heads_q, head_dim, grad_dtype).total;
+  if (batch < 1 || seqlen_q < 1 || seqlen_k < 1 || heads_q < 1 || heads_kv < 1 || head_dim < 1) return 0;
+  return bwd_layout(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype, grad_dtype).total;
 }
 
 mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -157,8 +162,7 @@ mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
   mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
                                  grad_dtype, causal, block_q, block_k, tau, softmax_scale);
   if (st != MALA_OK) return st;
-  if (bwd_simt_smem(in_dtype, head_dim, block_q) > 227u * 1024u) return MALA_ERR_UNSUPPORTED;
-  const BwdLayout w = bwd_layout(batch, seqlen_q, heads_q, head_dim, grad_dtype);
+  const BwdLayout w = bwd_layout(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype, grad_dtype);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
     return MALA_ERR_WORKSPACE;
   int* status = status_word();
@@ -172,11 +176,19 @@ mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
   a.scale_log2 = softmax_scale * kLog2e; a.scale = softmax_scale;
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.dq_acc = grad_dtype == MALA_FP32 ? static_cast<float*>(dq) : reinterpret_cast<float*>(ws + w.dq_acc);
+  a.scratch = ws + w.scratch;
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  const bool tc = bwd_tc_supported(a);
+  if (!tc && bwd_simt_smem(in_dtype, head_dim, block_q) > 227u * 1024u) return MALA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  cudaError_t e = launch_bwd_preprocess(a, s, &launches);
-  if (e == cudaSuccess) e = launch_bwd_simt(a, s, &launches);
+  cudaError_t e = cudaSuccess;
+  if (tc) {
+    e = launch_bwd_tc(a, s, &launches);
+  } else {
+    e = launch_bwd_preprocess(a, s, &launches);
+    if (e == cudaSuccess) e = launch_bwd_simt(a, s, &launches);
+  }
   if (e == cudaSuccess && grad_dtype == MALA_BF16) e = launch_dq_convert(a, s, &launches);
   return finish(e, launches);
 }

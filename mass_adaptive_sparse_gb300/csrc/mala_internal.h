@@ -68,6 +68,11 @@ cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t s, int* launches)
 // Tensor-core (tcgen05) kernels: bf16 inputs, head_dim 128, 128 x 128 tiles.
 bool fwd_tc_supported(const FwdArgs& a);
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches);
+bool bwd_tc_supported(const BwdArgs& a);
+// Workspace bytes of the fp16 operand copies the tensor-core backward makes.
+size_t bwd_tc_scratch_bytes(int B, int Lq, int Lk, int Hq, int Hkv, int D);
+// Preprocess (fp16 copies, D, zeroed dQ accumulator) + main kernel.
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches);
 
 // Shared-memory bytes the SIMT kernels need (0 = shape not supported).
 size_t fwd_simt_smem(int in_dt, int D, int blk);
