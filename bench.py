@@ -87,7 +87,7 @@ def decode_bytes(cfg, kept_tiles):
     n_tiles = cfg.B * cfg.Hkv * -(-cfg.N // cfg.block)
     k_bytes = n_tiles * tile
     v_bytes = kept_tiles * tile
-    other = cfg.B * cfg.H * cfg.d * 2 * 2 + cfg.num_splits * cfg.B * cfg.H * (cfg.d + 2) * 4 * 2
+    other = cfg.B * cfg.H * cfg.d * 2 * 2 + cfg.num_splits * cfg.B * cfg.H * (cfg.d + 4) * 4 * 2
     return k_bytes + v_bytes + other
 
 

@@ -176,7 +176,7 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
  *
  *  - The array holds mala_decode_noalloc_max_floats() floats (1 Mi floats,
  *    4 MiB) on every device that loads the library, until the process exits.
- *    A call needs num_splits * batch * heads_q * (head_dim + 2) floats; larger
+ *    A call needs num_splits * batch * heads_q * (head_dim + 4) floats; larger
  *    shapes return MALA_ERR_WORKSPACE before anything is launched.
  *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  *    library routine.

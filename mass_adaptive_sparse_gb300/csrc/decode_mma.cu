@@ -1,0 +1,352 @@
+// MALA split-KV decode, bandwidth-oriented (bf16, head_dim 128, 128-key tiles).
+//
+// "MassAlloc Attention: Let Attention Allocate Its Own Compute", App. A.1
+// ("Fused decoding execution") and §2.4: one query per sequence against its
+// KV cache; every tile is scored, and V is loaded and P V run only for tiles
+// the test of Eq. (3) keeps.  Each split starts from its own empty (m, l),
+// visits its tiles newest to oldest and tests against L = N (the full
+// context).  The G query heads sharing a KV head form the query block: a tile
+// is kept if any of them keeps it.  The split writes (m, l, l_rounded, u) for
+// the exact merge of "Why exact attention does not need a quadratic matrix".
+//
+// One CTA of 160 threads per (split, KV head, sequence):
+//   warp 4     TMA producer: K tiles, 3-stage ring, running ahead.
+//   warps 0-3  S^T = K q^T with mma.sync m16n8k16 (keys as M, the G <= 8 heads
+//              as N), row max per head, vote; for kept tiles thread 0 issues
+//              the V load, P (bf16) goes to a shared slot, and the P V product
+//              O^T += V^T P^T (warp w owns head dims 32w..32w+31) runs up to two
+//              kept tiles later, so each V load has two tiles of work to land.
+// The reference max m is moved lazily (only past 2^8 growth); every pending P
+// carries the m it was computed with, and O is rescaled to it before its P V.
+#include <cuda_bf16.h>
+
+#include "mala_internal.h"
+#include "tc_common.cuh"
+
+namespace mala {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 128;
+constexpr int kBK = 128;
+constexpr int kTile = kBK * kD * 2;
+constexpr int kHalf = kTile / 2;
+constexpr int kNK = 3;          // K ring
+constexpr int kNV = 3;          // V ring = pending P slots
+constexpr int kThreads = 160;
+constexpr int kSmem = kTile * (kNK + kNV) + 1024;
+constexpr float kRescale = 8.0f;
+
+struct Bars {
+  uint64_t k_full[kNK], k_empty[kNK];
+  uint64_t v_full[kNV];
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// smem byte address of 16-byte chunk `chunk` (8 bf16 along d) of row `row` in a
+// [128 rows x 128 d] tile stored as two 128-byte-swizzled 64-column halves.
+__device__ __forceinline__ uint32_t sw_addr(uint32_t base, int row, int dchunk) {
+  return base + (dchunk >> 3) * kHalf + row * 128 + (((dchunk & 7) ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const DecArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) Bars bars;
+  __shared__ int abort_flag;
+  __shared__ float red_max[2][4][8], red_sum[4][8], red_sumr[4][8];   // red_max double-buffered by tile
+  __shared__ __align__(16) uint16_t pslot[kNV][8][kBK];   // P (bf16) of pending kept tiles, [head][key]
+  __shared__ float pslot_m[kNV][8];                         // reference max each P was taken against
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sK = base, sV = base + kNK * kTile;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int sp = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int G = a.Hq / a.Hkv;
+  const int T = (a.N + kBK - 1) / kBK;
+  const int per = (T + a.splits - 1) / a.splits;
+  const int t0 = sp * per, t1 = min(T, t0 + per);
+  const int ntiles = max(0, t1 - t0);
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kNK; ++i) { mbar_init(smem_u32(&bars.k_full[i]), 1); mbar_init(smem_u32(&bars.k_empty[i]), 1); }
+    for (int i = 0; i < kNV; ++i) mbar_init(smem_u32(&bars.v_full[i]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abortp = &abort_flag;
+
+  if (warp == 4) {
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kNK, n = t / kNK;
+        if (n > 0 && !mbar_wait(smem_u32(&bars.k_empty[s]), (n - 1) & 1, abortp, a.status)) break;
+        const int row = (t1 - 1 - t) * kBK;                 // newest tile first
+        const uint32_t kf = smem_u32(&bars.k_full[s]);
+        mbar_expect_tx(kf, kTile);
+        tma_load_4d(sK + s * kTile, &mk, kf, 0, hk, row, b);
+        tma_load_4d(sK + s * kTile + kHalf, &mk, kf, 64, hk, row, b);
+        ++issued;
+      }
+      for (int t = max(0, issued - kNK); t < issued; ++t)
+        mbar_wait(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, abortp, a.status);
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
+  const bool test = a.tau > 0.f;
+  const float thr = a.log2_tau - log2f(static_cast<float>(a.N));
+  const float sl2 = a.scale_log2;
+  const int gq = lane >> 2, cq = lane & 3;       // fragment row group / column pair
+
+  // q^T as the B operand (K = d, N = heads): b0b1 = q[head gq][16k + 2cq ..], b2b3 = q[gq][16k + 8 + 2cq ..]
+  uint32_t qb[8][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                             (static_cast<size_t>(b) * a.Hq + hk * G + gq) * kD);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      qb[k][0] = gq < G ? qrow[(16 * k + 2 * cq) / 2] : 0u;
+      qb[k][1] = gq < G ? qrow[(16 * k + 8 + 2 * cq) / 2] : 0u;
+    }
+  }
+  float m_ref[8], l_ex[8], l_rd[8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) { m_ref[g] = -INFINITY; l_ex[g] = 0.f; l_rd[g] = 0.f; }
+  float m_o0 = -INFINITY, m_o1 = -INFINITY;   // reference max of this thread's O columns (heads 2cq, 2cq+1)
+  float o[2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+  int nret = 0, npv = 0, kept = 0;
+  bool ok = true;
+
+  // O^T += V^T P^T for the pending kept tile number n
+  auto pv = [&](int n) {
+    const int vs = n % kNV;
+    ok = ok && mbar_wait(smem_u32(&bars.v_full[vs]), (n / kNV) & 1, abortp, a.status);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    // rescale O to the reference max this P was taken against
+    const float mn0 = pslot_m[vs][(2 * cq) & 7], mn1 = pslot_m[vs][(2 * cq + 1) & 7];
+    const float f0 = (m_o0 == -INFINITY) ? 0.f : ex2(m_o0 - mn0);
+    const float f1 = (m_o1 == -INFINITY) ? 0.f : ex2(m_o1 - mn1);
+    if (mn0 != -INFINITY) { o[0][0] *= f0; o[0][2] *= f0; o[1][0] *= f0; o[1][2] *= f0; m_o0 = mn0; }
+    if (mn1 != -INFINITY) { o[0][1] *= f1; o[0][3] *= f1; o[1][1] *= f1; o[1][3] *= f1; m_o1 = mn1; }
+    const uint32_t vbase = sV + vs * kTile;
+    const uint32_t* prow = reinterpret_cast<const uint32_t*>(&pslot[vs][gq][0]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t b0 = prow[(16 * k + 2 * cq) / 2];
+      const uint32_t b1 = prow[(16 * k + 8 + 2 * cq) / 2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        // A = V^T (16 d x 16 keys): four 8x8 transposed loads
+        const int key = 16 * k + (lane & 7) + 8 * (lane >> 4);
+        const int dchunk = (32 * warp + 16 * mt) / 8 + ((lane >> 3) & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(sw_addr(vbase, key, dchunk), a0, a1, a2, a3);
+        mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+    ++npv;
+  };
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int j = t1 - 1 - t;
+    const int s = t % kNK;
+    ok = ok && mbar_wait(smem_u32(&bars.k_full[s]), (t / kNK) & 1, abortp, a.status);
+    // S^T for this warp's 32 keys: acc[mt] = rows (keys) 32w + 16mt + {gq, gq+8}, cols (heads) {2cq, 2cq+1}
+    float acc[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+    if (__all_sync(0xffffffffu, ok)) {
+      const uint32_t kbase = sK + s * kTile;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int key = 32 * warp + 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int dchunk = 2 * k + (lane >> 4);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(sw_addr(kbase, key, dchunk), a0, a1, a2, a3);
+          mma_bf16(acc[mt], a0, a1, a2, a3, qb[k][0], qb[k][1]);
+        }
+      }
+    }
+    // mask keys beyond the cache, row max per head
+    const int kbase_idx = j * kBK + 32 * warp;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const bool valid = kbase_idx + 16 * mt + gq + 8 * hrow < a.N;
+        acc[mt][2 * hrow] = valid ? acc[mt][2 * hrow] * sl2 : -INFINITY;
+        acc[mt][2 * hrow + 1] = valid ? acc[mt][2 * hrow + 1] * sl2 : -INFINITY;
+        mx0 = fmaxf(mx0, acc[mt][2 * hrow]);
+        mx1 = fmaxf(mx1, acc[mt][2 * hrow + 1]);
+      }
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    if (gq == 0) { red_max[t & 1][warp][2 * cq] = mx0; red_max[t & 1][warp][2 * cq + 1] = mx1; }
+    if (named_vote_or(1, 128, !ok || *abortp)) break;      // also the barrier for red_max / K reads
+    if (tid == 0) mbar_arrive(smem_u32(&bars.k_empty[s]));
+    float mt_h[8];
+    int keep = !test;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      mt_h[g] = fmaxf(fmaxf(red_max[t & 1][0][g], red_max[t & 1][1][g]), fmaxf(red_max[t & 1][2][g], red_max[t & 1][3][g]));
+      if (g < G && test && (l_ex[g] == 0.f || !(mt_h[g] - m_ref[g] - lg2(l_ex[g]) < thr))) keep = 1;
+    }
+    if (a.mask != nullptr && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * T + j] = keep ? 1 : 0;
+    if (keep) {
+      ++kept;
+      const int vs = nret % kNV;
+      if (tid == 0) {
+        // V of this tile: loaded only now that the tile is kept; its slot was
+        // freed by the P V of kept tile nret - kNV, finished before the barrier above
+        const uint32_t vf = smem_u32(&bars.v_full[vs]);
+        mbar_expect_tx(vf, kTile);
+        tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBK, b);
+        tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBK, b);
+      }
+      // lazily moved reference max, then P = exp2(s - m) as bf16 into the slot
+      float alpha[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        alpha[g] = 1.f;
+        if (mt_h[g] > m_ref[g] + kRescale) {
+          alpha[g] = (m_ref[g] == -INFINITY) ? 0.f : ex2(m_ref[g] - mt_h[g]);
+          m_ref[g] = mt_h[g];
+        }
+      }
+      const float mr0 = m_ref[2 * cq] == -INFINITY ? 0.f : m_ref[2 * cq];
+      const float mr1 = m_ref[2 * cq + 1] == -INFINITY ? 0.f : m_ref[2 * cq + 1];
+      float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int hrow = 0; hrow < 2; ++hrow) {
+          const int key = 32 * warp + 16 * mt + gq + 8 * hrow;
+          const float p0 = ex2(acc[mt][2 * hrow] - mr0);
+          const float p1 = ex2(acc[mt][2 * hrow + 1] - mr1);
+          const uint32_t w = pack_bf16(p0, p1);
+          se0 += p0; se1 += p1;
+          sr0 += __uint_as_float(w << 16);
+          sr1 += __uint_as_float(w & 0xffff0000u);
+          if (2 * cq < 8) pslot[vs][2 * cq][key] = static_cast<uint16_t>(w & 0xffffu);
+          if (2 * cq + 1 < 8) pslot[vs][2 * cq + 1][key] = static_cast<uint16_t>(w >> 16);
+        }
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        se0 += __shfl_xor_sync(0xffffffffu, se0, off);
+        se1 += __shfl_xor_sync(0xffffffffu, se1, off);
+        sr0 += __shfl_xor_sync(0xffffffffu, sr0, off);
+        sr1 += __shfl_xor_sync(0xffffffffu, sr1, off);
+      }
+      if (gq == 0) {
+        red_sum[warp][2 * cq] = se0; red_sum[warp][2 * cq + 1] = se1;
+        red_sumr[warp][2 * cq] = sr0; red_sumr[warp][2 * cq + 1] = sr1;
+      }
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        if (tid == g) pslot_m[vs][g] = m_ref[g];
+      named_sync(1, 128);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        l_ex[g] = l_ex[g] * alpha[g] + (red_sum[0][g] + red_sum[1][g] + red_sum[2][g] + red_sum[3][g]);
+        l_rd[g] = l_rd[g] * alpha[g] + (red_sumr[0][g] + red_sumr[1][g] + red_sumr[2][g] + red_sumr[3][g]);
+      }
+      ++nret;
+      // keep at most kNV - 1 products pending; the oldest runs now
+      if (nret - npv >= kNV) pv(npv);
+      named_sync(1, 128);        // red_sum reads done before the next tile overwrites them
+    }
+  }
+  while (npv < nret && __all_sync(0xffffffffu, ok) && !*abortp) pv(npv);
+
+  // split record: (m, l, l_rounded, 0, u[D]) per query head, m in log2 units
+  if (__all_sync(0xffffffffu, ok && !*abortp)) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int d = 32 * warp + 16 * mt + gq + 8 * hrow;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int g = 2 * cq + e;
+          if (g < G) {
+            float* rec = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (kD + 4);
+            rec[4 + d] = o[mt][2 * hrow + e];
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (tid == g && g < G) {
+        float* rec = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (kD + 4);
+        rec[0] = m_ref[g];
+        rec[1] = l_ex[g];
+        rec[2] = l_rd[g];
+        rec[3] = 0.f;
+      }
+    }
+    if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+  }
+  // V loads issued but never consumed (abort path) must land before exit
+  if (tid == 0)
+    for (int n = npv; n < nret; ++n) mbar_wait(smem_u32(&bars.v_full[n % kNV]), (n / kNV) & 1, abortp, a.status);
+}
+
+}  // namespace
+
+bool decode_mma_supported(const DecArgs& a) {
+  return a.in_dt == kBF16 && a.D == kD && a.blk == kBK && a.Hq / a.Hkv <= 8;
+}
+
+cudaError_t launch_decode_mma(const DecArgs& a, cudaStream_t s, int* launches) {
+  CUtensorMap mk, mv;
+  if (!encode_bshd_map(&mk, a.k, a.B, a.N, a.Hkv, kD, kBK) || !encode_bshd_map(&mv, a.v, a.B, a.N, a.Hkv, kD, kBK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.splits, a.Hkv, a.B);
+  ++*launches;
+  decode_mma_kernel<<<grid, kThreads, kSmem, s>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace mala

@@ -195,7 +195,7 @@ mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
 
 size_t mala_decode_workspace_size(int batch, int heads_q, int head_dim, int num_splits) {
   if (batch < 1 || heads_q < 1 || head_dim < 1 || num_splits < 1) return 0;
-  return round256(static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 2) * sizeof(float));
+  return round256(static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 4) * sizeof(float));
 }
 
 mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache, void* o,
@@ -233,7 +233,7 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  cudaError_t e = launch_decode_simt(a, s, &launches);
+  cudaError_t e = decode_mma_supported(a) ? launch_decode_mma(a, s, &launches) : launch_decode_simt(a, s, &launches);
   if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
   return finish(e, launches);
 }
@@ -257,7 +257,7 @@ mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* 
   if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
   if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
-  const size_t need = static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 2);
+  const size_t need = static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 4);
   if (need > kNoAllocDecodeFloats) return MALA_ERR_WORKSPACE;
   float* scratch = decode_scratch();
   int* status = status_word();
@@ -272,7 +272,7 @@ mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* 
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  cudaError_t e = launch_decode_simt(a, s, &launches);
+  cudaError_t e = decode_mma_supported(a) ? launch_decode_mma(a, s, &launches) : launch_decode_simt(a, s, &launches);
   if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
   return finish(e, launches);
 }

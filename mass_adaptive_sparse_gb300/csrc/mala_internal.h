@@ -51,7 +51,8 @@ struct DecArgs {
   int B, N, Hq, Hkv, D;
   int in_dt, out_dt, blk, splits;
   float tau, log2_tau, scale_log2;
-  float* partial;       // workspace: [splits, B, Hq, D + 2] = (m, l, u[D]) in log2 units
+  float* partial;       // workspace: [splits, B, Hq, D + 4] = (m, l, l_rounded, 0, u[D]), m in log2 units;
+                        // l sums P exactly, l_rounded sums P as rounded for the P V product
   int32_t* counts;      // [B, Hkv, splits] or null
   uint8_t* mask;        // [B, Hkv, T] or null
   int* status;
@@ -73,6 +74,8 @@ bool bwd_tc_supported(const BwdArgs& a);
 size_t bwd_tc_scratch_bytes(int B, int Lq, int Lk, int Hq, int Hkv, int D);
 // Preprocess (fp16 copies, D, zeroed dQ accumulator) + main kernel.
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches);
+bool decode_mma_supported(const DecArgs& a);
+cudaError_t launch_decode_mma(const DecArgs& a, cudaStream_t s, int* launches);
 
 // Shared-memory bytes the SIMT kernels need (0 = shape not supported).
 size_t fwd_simt_smem(int in_dt, int D, int blk);

@@ -440,36 +440,42 @@ decode_split_simt_kernel(const DecArgs a) {
   for (int c = tid; c < D; c += NT) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float* pp = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (D + 2);
-      if (c == 0) { pp[0] = m[g]; pp[1] = l[g]; }
-      pp[2 + c] = u[g];
+      float* pp = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (D + 4);
+      if (c == 0) { pp[0] = m[g]; pp[1] = l[g]; pp[2] = l[g]; pp[3] = 0.f; }   // P is not rounded here
+      pp[4 + c] = u[g];
     }
   }
   if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
 }
 
 // Exact merge of the splits' (m, l, u): one CTA per (query head, batch).
+// o = sum_s e^(m_s - M) u_s / sum_s e^(m_s - M) l_rounded_s (the sums of the P
+// values that entered the P V products); lse = M + log sum_s e^(m_s - M) l_s.
 template <typename Tout>
 __global__ void decode_merge_kernel(const DecArgs a) {
   const int h = blockIdx.x, b = blockIdx.y;
   const int D = a.D;
-  const size_t stride = static_cast<size_t>(a.B) * a.Hq * (D + 2);
-  const float* base = a.partial + (static_cast<size_t>(b) * a.Hq + h) * (D + 2);
+  const size_t stride = static_cast<size_t>(a.B) * a.Hq * (D + 4);
+  const float* base = a.partial + (static_cast<size_t>(b) * a.Hq + h) * (D + 4);
   float mmax = -INFINITY;
   for (int s = 0; s < a.splits; ++s)
     if (base[s * stride + 1] > 0.f) mmax = fmaxf(mmax, base[s * stride]);
-  float lsum = 0.f;
+  float lsum = 0.f, lrsum = 0.f;
   for (int s = 0; s < a.splits; ++s) {
     const float ls = base[s * stride + 1];
-    if (ls > 0.f) lsum += exp2f(base[s * stride] - mmax) * ls;
+    if (ls > 0.f) {
+      const float w = exp2f(base[s * stride] - mmax);
+      lsum += w * ls;
+      lrsum += w * base[s * stride + 2];
+    }
   }
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     float u = 0.f;
     for (int s = 0; s < a.splits; ++s) {
       const float ls = base[s * stride + 1];
-      if (ls > 0.f) u += exp2f(base[s * stride] - mmax) * base[s * stride + 2 + c];
+      if (ls > 0.f) u += exp2f(base[s * stride] - mmax) * base[s * stride + 4 + c];
     }
-    st(static_cast<Tout*>(a.o) + (static_cast<size_t>(b) * a.Hq + h) * D + c, u / lsum);
+    st(static_cast<Tout*>(a.o) + (static_cast<size_t>(b) * a.Hq + h) * D + c, u / lrsum);
   }
   if (threadIdx.x == 0) a.lse[static_cast<size_t>(b) * a.Hq + h] = (mmax + log2f(lsum)) * kLn2;
 }

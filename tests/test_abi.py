@@ -49,7 +49,7 @@ def test_workspace_sizes(lib):
     assert ws_bf16 >= ws_f32 + B * L * H * D * 4
     assert lib.mala_bwd_workspace_size(0, L, L, H, H, D, 0, 1) == 0
     dec = lib.mala_decode_workspace_size(8, 32, 128, 16)
-    assert dec >= 16 * 8 * 32 * 130 * 4 and dec % 256 == 0
+    assert dec >= 16 * 8 * 32 * 132 * 4 and dec % 256 == 0
     assert lib.mala_decode_workspace_size(8, 32, 128, 0) == 0
 
 
@@ -95,7 +95,7 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 def test_noalloc_decode_rejects_oversize_before_any_launch(lib):
     cap = lib.mala_decode_noalloc_max_floats()
     assert cap == 1 << 20
-    # 16 splits * 64 sequences * 32 heads * 130 floats > cap: rejected by shape alone
+    # 16 splits * 64 sequences * 32 heads * 132 floats > cap: rejected by shape alone
     rc = lib.mala_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 1024, 32, 8, 128, 0, 0, 128, 16, 1.0, 0.08,
                                  None, None, None)
     assert rc == 3
