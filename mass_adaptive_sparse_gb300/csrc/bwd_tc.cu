@@ -14,10 +14,14 @@
 // dO made by the preprocess kernel); P and dS are rounded to fp16, which keeps
 // the gradients within 2e-4 mean relative error where bf16 would not.
 //
-// 192 threads: warps 0-3 = "math" warpgroup (thread r owns key row r = TMEM
-// lane r for S^T, P^T, dP^T, dV, dK, and query row r for the dQ read-out),
-// warp 4 = TMA producer (K, V once; Q ring), warp 5 = MMA issuer.
-// TMEM columns: [0,128) S^T then P^T (fp16 in [0,64)); [128,256) dP^T then
+// 320 threads: warps 0-7 = two "math" warpgroups; thread (c, r) of group c
+// owns key row r = TMEM lane r and the 64 query columns [64c, 64c + 64) of
+// S^T, P^T, dP^T and dS (and, for the dQ read-out, query row r with head
+// dims [64c, 64c + 64)); warp 8 = TMA producer (K, V once; Q ring); warp 9 =
+// MMA issuer.  dS is stored pre-multiplied by the softmax scale, so dQ and dK
+// come out of the products already scaled.
+// TMEM columns: [0,128) S^T then P^T (fp16: queries 0-63 in [0,32), 64-127 in
+// [64,96)); [128,256) dP^T then
 // dQ; [256,384) dV; [384,512) dK.  dS is written to shared memory once, in the
 // 128-byte-swizzled layout that is K-major for dK = dS^T Q (A = dS^T) and
 // MN-major for dQ = dS K (A = dS).
@@ -38,7 +42,8 @@ constexpr int kD = 128;
 constexpr int kBlk = 128;
 constexpr int kTile = kBlk * kD * 2;    // 32 KiB of fp16
 constexpr int kHalf = kTile / 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kMath = 256;            // two math warpgroups
 // shared memory: K, V, Q[2], dO, dS
 constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile;
 constexpr int kSmem = 6 * kTile + 1024;
@@ -102,7 +107,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   __shared__ uint32_t tmem_sh;
   __shared__ int flag;
   __shared__ int abort_flag;
-  __shared__ float vec_lse[2][kBlk], vec_d[2][kBlk], vec_c[2][kBlk];
+  __shared__ __align__(16) float vec_lse[2][kBlk], vec_d[2][kBlk], vec_c[2][kBlk];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO, sDS = base + kOffDS;
@@ -139,7 +144,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t tmem = tmem_sh;
   volatile int* abortp = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer: K, V once; Q ring of 2 ----------------
     if (lane == 0) {
       prefetch_tensormap(&mq);
@@ -167,7 +172,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       for (int t = max(0, issued - 2); t < issued; ++t)
         mbar_wait(smem_u32(&bars.q_full[t & 1]), (t >> 1) & 1, abortp, a.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_f16(0, 0, 0, kBlk, kBlk);    // A, B K-major (fp16)
@@ -205,11 +210,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mma_ss(tmem + kColDP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
           }
           mma_commit(smem_u32(&bars.dp_full));
-          // dV += P^T dO   (A = P^T from TMEM)
+          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
+          // queries 64-127 in columns 64-95, each written by its math group)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColDV, tmem + kColS + k * 8, desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn,
-                   (nret > 0 || k > 0) ? 1u : 0u);
+            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
+                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars.do_empty));
         }
         if (t + 1 < ntiles && !issue_qk(t + 1)) break;
@@ -237,11 +243,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_wait(smem_u32(&bars.fin), 0, abortp, a.status);
     }
   } else {
-    // ---------------- math warpgroup ----------------
-    const int r = tid;
+    // ---------------- math warpgroups ----------------
+    const int r = tid & 127;                    // key row = TMEM lane
+    const int cg = tid >> 7;                    // column group: queries / head dims [64cg, 64cg + 64)
     const int key = kb * kBlk + r;
     const bool key_ok = key < a.Lk;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool keys_full = kb * kBlk + kBlk <= a.Lk;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool test = a.tau > 0.f;
     const float sl2 = a.scale_log2;
     const float inv_sl2 = 1.f / sl2;
@@ -249,7 +257,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     bool ok = true;
     int prev_q0 = 0, prev_h = 0;   // query block / head of the last retained tile (for the dQ read-out)
 
-    // per-query vectors of tile t: lse (log2 units), D, decision threshold in raw dot units
+    // per-query vectors of tile t (fetched by group 0): lse (log2 units), D,
+    // and the decision threshold in raw dot units (keep iff raw S >= c)
     float n_lse = 0.f, n_d = 0.f, n_c = 0.f;
     auto fetch = [&](int t) {
       const int h = hk * G + t / ni, i = ibot + t % ni;
@@ -260,28 +269,28 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         n_d = a.delta[off];
         const float thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
                                : -INFINITY;
-        n_c = (n_lse + thr) * inv_sl2;        // keep iff raw S >= n_c
+        n_c = (n_lse + thr) * inv_sl2;
       } else {
         n_lse = 0.f; n_d = 0.f; n_c = INFINITY;
       }
     };
-    if (ntiles > 0) fetch(0);
+    if (ntiles > 0 && cg == 0) fetch(0);
 
     auto readout_dq = [&](int which) {      // add the finished dQ tile into the fp32 accumulator
       ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
       fence_after_sync();
       if (__all_sync(0xffffffffu, ok)) {
         const int q = prev_q0 + r;
-        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + (q < a.Lq ? q : 0)) * a.Hq + prev_h) * kD;
+        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + (q < a.Lq ? q : 0)) * a.Hq + prev_h) * kD + 64 * cg;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32_sync(lane_addr + kColDP + c * 32, v);
+          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
           if (q < a.Lq) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + c * 32 + e, __uint_as_float(v[e]) * a.scale, __uint_as_float(v[e + 1]) * a.scale,
-                         __uint_as_float(v[e + 2]) * a.scale, __uint_as_float(v[e + 3]) * a.scale);
+              red_add_v4(dst + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                         __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
           }
         }
       }
@@ -292,37 +301,51 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int h = hk * G + t / ni, i = ibot + t % ni;
       const int q0 = i * kBlk;
       const int vb = t & 1;
-      vec_lse[vb][r] = n_lse;
-      vec_d[vb][r] = n_d;
-      vec_c[vb][r] = n_c;
-      named_sync(1, 128);
-      if (t + 1 < ntiles) fetch(t + 1);
+      if (cg == 0) {
+        vec_lse[vb][r] = n_lse;
+        vec_d[vb][r] = n_d;
+        vec_c[vb][r] = n_c;
+      }
+      named_sync(1, kMath);
+      if (cg == 0 && t + 1 < ntiles) fetch(t + 1);
 
       ok = mbar_wait(smem_u32(&bars.s_full), t & 1, abortp, a.status);
       fence_after_sync();
-      // Eq. (4): keep iff some valid entry has S - lse >= log(tau / L_q).  S^T is
-      // read from TMEM 32 columns at a time (again below for P if retained).
+      // Eq. (4): keep iff some valid entry has S - lse >= log(tau / L_q)
       const bool diag = a.causal && q0 == kb * kBlk;
       const int qlim = a.Lq - q0;                 // query columns at or beyond this are out of range
       const int qmin = diag ? r : 0;              // causal: query >= key inside the diagonal tile
+      const bool interior = !diag && qlim >= kBlk && keys_full;
+      const float4* c4 = reinterpret_cast<const float4*>(&vec_c[vb][64 * cg]);
       int keep_row = 0;
       if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t sr[32];
-          tmem_ld32_sync(lane_addr + kColS + c * 32, sr);
+          tmem_ld32_sync(lane_addr + kColS + 64 * cg + c * 32, sr);
+          float gap = -INFINITY;
+          if (interior) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int q = c * 32 + e;
-            keep_row |= (key_ok && q < qlim && q >= qmin && __uint_as_float(sr[e]) >= vec_c[vb][q]) ? 1 : 0;
+            for (int e = 0; e < 32; e += 4) {
+              const float4 cc = c4[(c * 32 + e) / 4];
+              gap = fmaxf(gap, fmaxf(fmaxf(__uint_as_float(sr[e]) - cc.x, __uint_as_float(sr[e + 1]) - cc.y),
+                                     fmaxf(__uint_as_float(sr[e + 2]) - cc.z, __uint_as_float(sr[e + 3]) - cc.w)));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int q = 64 * cg + c * 32 + e;
+              if (key_ok && q < qlim && q >= qmin) gap = fmaxf(gap, __uint_as_float(sr[e]) - vec_c[vb][q]);
+            }
           }
+          keep_row |= gap >= 0.f ? 1 : 0;
         }
       }
       fence_before_sync();
-      const int keep = named_vote_or(1, 128, keep_row);
-      if (named_vote_or(1, 128, !ok || *abortp)) break;
+      const int keep = named_vote_or(1, kMath, keep_row);
+      if (named_vote_or(1, kMath, !ok || *abortp)) break;
       uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + i) * Tc + kb : nullptr;
-      if (r == 0) {
+      if (tid == 0) {
         head_kept += keep;
         if (t % ni == ni - 1) {                   // last query block of this head
           if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tc + kb] = head_kept;
@@ -330,14 +353,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
       }
       if (!keep) {
-        if (r == 0) {
+        if (tid == 0) {
           if (mrow) *mrow = 0;
           flag = 0;
           mbar_arrive(smem_u32(&bars.p_ready));
         }
         continue;
       }
-      if (r == 0) {
+      if (tid == 0) {
         if (mrow) *mrow = 1;
         // dO of this tile, loaded only now that the tile is retained
         if (nret > 0) ok = mbar_wait(smem_u32(&bars.do_empty), (nret - 1) & 1, abortp, a.status);
@@ -349,60 +372,72 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           ++do_issued;
         }
       }
-      // P^T = exp2(S * scale_log2 - lse) in fp16, over S's columns
-      // P^T = exp2(S * scale_log2 - lse) in fp16, written over S's first 64 columns
-      uint32_t pk[64];
+      // P^T = exp2(S * scale_log2 - lse) in fp16, written over this group's S columns
+      const float4* l4 = reinterpret_cast<const float4*>(&vec_lse[vb][64 * cg]);
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t sr[32];
-        tmem_ld32_sync(lane_addr + kColS + c * 32, sr);
+        tmem_ld32_sync(lane_addr + kColS + 64 * cg + c * 32, sr);
+        if (interior) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = c * 32 + 2 * e;
-          const bool l0 = key_ok && q < qlim && q >= qmin;
-          const bool l1 = key_ok && q + 1 < qlim && q + 1 >= qmin;
-          const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[2 * e]), sl2, -vec_lse[vb][q])) : 0.f;
-          const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -vec_lse[vb][q + 1])) : 0.f;
-          pk[c * 16 + e] = pack_f16(p0, p1);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 ll = l4[(c * 32 + e) / 4];
+            pk[c * 16 + e / 2] = pack_f16(ex2(fmaf(__uint_as_float(sr[e]), sl2, -ll.x)),
+                                          ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -ll.y)));
+            pk[c * 16 + e / 2 + 1] = pack_f16(ex2(fmaf(__uint_as_float(sr[e + 2]), sl2, -ll.z)),
+                                              ex2(fmaf(__uint_as_float(sr[e + 3]), sl2, -ll.w)));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q = 64 * cg + c * 32 + e;
+            const bool l0 = key_ok && q < qlim && q >= qmin;
+            const bool l1 = key_ok && q + 1 < qlim && q + 1 >= qmin;
+            const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -vec_lse[vb][q])) : 0.f;
+            const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -vec_lse[vb][q + 1])) : 0.f;
+            pk[c * 16 + e / 2] = pack_f16(p0, p1);
+          }
         }
       }
-      tmem_st32(lane_addr + kColS, pk);
-      tmem_st32(lane_addr + kColS + 32, pk + 32);
+      tmem_st32(lane_addr + kColS + 64 * cg, pk);   // inside this group's own S columns
       tmem_st_wait();
       fence_before_sync();
-      if (named_vote_or(1, 128, !ok || *abortp)) break;
-      if (r == 0) {
+      if (named_vote_or(1, kMath, !ok || *abortp)) break;
+      if (tid == 0) {
         flag = 1;
         mbar_arrive(smem_u32(&bars.p_ready));
       }
       // dQ of the previous retained tile leaves the dP columns before dP^T lands there
       if (nret > 0) {
         readout_dq(nret - 1);
-        if (named_vote_or(1, 128, !ok || *abortp)) break;
-        if (r == 0) mbar_arrive(smem_u32(&bars.dq_free));
+        if (named_vote_or(1, kMath, !ok || *abortp)) break;
+        if (tid == 0) mbar_arrive(smem_u32(&bars.dq_free));
       }
       ok = mbar_wait(smem_u32(&bars.dp_full), nret & 1, abortp, a.status);
       fence_after_sync();
-      // dS^T = P^T o (dP^T - D), fp16, into the swizzled dS tile (row = key r)
+      // dS^T = scale * P^T o (dP^T - D), fp16, into half cg of the swizzled dS tile (row = key r)
       if (__all_sync(0xffffffffu, ok)) {
+        const float4* d4 = reinterpret_cast<const float4*>(&vec_d[vb][64 * cg]);
+        const float sc = a.scale;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t dp[32];
-          tmem_ld32_sync(lane_addr + kColDP + c * 32, dp);
+          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, dp);
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int q = c * 32 + 2 * e;
-            const uint32_t pw = pk[c * 16 + e];
-            const float ds0 = f16_lo(pw) * (__uint_as_float(dp[2 * e]) - vec_d[vb][q]);
-            const float ds1 = f16_hi(pw) * (__uint_as_float(dp[2 * e + 1]) - vec_d[vb][q + 1]);
-            w[e] = pack_f16(ds0, ds1);
+          for (int e = 0; e < 16; e += 2) {
+            const float4 dd = d4[(c * 32 + 2 * e) / 4];
+            const uint32_t pw0 = pk[c * 16 + e], pw1 = pk[c * 16 + e + 1];
+            w[e] = pack_f16(sc * f16_lo(pw0) * (__uint_as_float(dp[2 * e]) - dd.x),
+                            sc * f16_hi(pw0) * (__uint_as_float(dp[2 * e + 1]) - dd.y));
+            w[e + 1] = pack_f16(sc * f16_lo(pw1) * (__uint_as_float(dp[2 * e + 2]) - dd.z),
+                                sc * f16_hi(pw1) * (__uint_as_float(dp[2 * e + 3]) - dd.w));
           }
-          // queries c*32 .. c*32+31 -> 4 chunks of 8 in the 64-query half (c / 2)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int chunk = (c % 2) * 4 + u;          // 16-byte chunk inside the 128-byte row
-            const uint32_t addr = sDS + (c / 2) * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
+            const int chunk = c * 4 + u;                 // 16-byte chunk (8 queries) inside the 128-byte row
+            const uint32_t addr = sDS + cg * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                          :: "r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
                          : "memory");
@@ -411,8 +446,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       fence_proxy_async_smem();
       fence_before_sync();
-      if (named_vote_or(1, 128, !ok || *abortp)) break;
-      if (r == 0) mbar_arrive(smem_u32(&bars.ds_ready));
+      if (named_vote_or(1, kMath, !ok || *abortp)) break;
+      if (tid == 0) mbar_arrive(smem_u32(&bars.ds_ready));
       prev_q0 = q0;
       prev_h = h;
       ++nret;
@@ -422,25 +457,25 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (nret > 0 && __all_sync(0xffffffffu, ok && !*abortp)) readout_dq(nret - 1);
     fence_after_sync();
     if (__all_sync(0xffffffffu, ok && !*abortp)) {
-      const size_t off = ((static_cast<size_t>(b) * a.Lk + (key_ok ? key : 0)) * a.Hkv + hk) * kD;
+      const size_t off = ((static_cast<size_t>(b) * a.Lk + (key_ok ? key : 0)) * a.Hkv + hk) * kD + 64 * cg;
       Tg* dvp = static_cast<Tg*>(a.dv) + off;
       Tg* dkp = static_cast<Tg*>(a.dk) + off;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         if (nret > 0) {
-          tmem_ld32_sync(lane_addr + kColDV + c * 32, v);
+          tmem_ld32_sync(lane_addr + kColDV + 64 * cg + c * 32, v);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
         if (key_ok) store_grad_row<Tg>(dvp + c * 32, v, 1.f);
-        if (nret > 0) tmem_ld32_sync(lane_addr + kColDK + c * 32, v);
-        if (key_ok) store_grad_row<Tg>(dkp + c * 32, v, a.scale);
+        if (nret > 0) tmem_ld32_sync(lane_addr + kColDK + 64 * cg + c * 32, v);
+        if (key_ok) store_grad_row<Tg>(dkp + c * 32, v, 1.f);
       }
     }
     // a dO load issued for an abandoned tile must land before the CTA exits
-    if (r == 0 && *abortp && do_issued > 0)
+    if (tid == 0 && *abortp && do_issued > 0)
       mbar_wait(smem_u32(&bars.do_full), (do_issued - 1) & 1, abortp, a.status);
     fence_before_sync();
   }
