@@ -8,7 +8,8 @@
 // on every valid causal entry.  A skipped tile loads no dO and runs no
 // post-score work.  A retained tile runs
 //   P^T = exp(S^T - lse), dP^T = V dO^T, dS^T = P^T o (dP^T - D),
-//   dV += P^T dO, dK += dS^T Q, dQ += dS K  (dQ added to an fp32 accumulator).
+//   dV += P^T dO, dK += dS^T Q, dQ += dS K  (formed as dQ^T = K^T dS^T and
+//   added to an fp32 accumulator).
 //
 // All post-score products run on fp16 operands (exact fp16 copies of Q, K, V,
 // dO made by the preprocess kernel); P and dS are rounded to fp16, which keeps
@@ -16,8 +17,8 @@
 //
 // 320 threads: warps 0-7 = two "math" warpgroups; thread (c, r) of group c
 // owns key row r = TMEM lane r and the 64 query columns [64c, 64c + 64) of
-// S^T, P^T, dP^T and dS (and, for the dQ read-out, query row r with head
-// dims [64c, 64c + 64)); warp 8 = TMA producer (K, V once; Q ring); warp 9 =
+// S^T, P^T, dP^T and dS (and, for the dQ^T read-out, head dim r of those 64
+// queries); warp 8 = TMA producer (K, V once; Q ring); warp 9 =
 // MMA issuer.  dS is stored pre-multiplied by the softmax scale, so dQ and dK
 // come out of the products already scaled.
 // TMEM columns: [0,128) S^T then P^T (fp16: queries 0-63 in [0,32), 64-127 in
@@ -57,9 +58,9 @@ struct Bars {
   uint64_t fin;
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" :: "l"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))); }
@@ -231,11 +232,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           mma_ss(tmem + kColDK, desc_kmajor_sw128(sDS + (k / 4) * kHalf + (k % 4) * 32),
                  desc_mnmajor_sw128(qb + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bars.q_empty[t & 1]));
-        // dQ = dS K   (A = dS: MN-major view of the same tile), into the dP columns
+        // dQ^T = K^T dS^T  (A = K tile read MN-major, B = the same dS tile read
+        // MN-major), into the dP columns: TMEM lane = head dim, column = query,
+        // so the read-out below adds whole 128-byte rows of dQ at once
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + kColDP, desc_mnmajor_sw128(sDS + k * 2048, kHalf, 1024),
-                 desc_mnmajor_sw128(sK + k * 2048, kHalf, 1024), id_mnmn, k > 0);
+          mma_ss(tmem + kColDP, desc_mnmajor_sw128(sK + k * 2048, kHalf, 1024),
+                 desc_mnmajor_sw128(sDS + k * 2048, kHalf, 1024), id_mnmn, k > 0);
         mma_commit(smem_u32(&bars.dq_full));
         ++nret;
       }
@@ -276,21 +279,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     };
     if (ntiles > 0 && cg == 0) fetch(0);
 
-    auto readout_dq = [&](int which) {      // add the finished dQ tile into the fp32 accumulator
+    // add the finished dQ^T tile (lane = head dim r, columns = queries) into the
+    // fp32 accumulator: for each query, the 32 lanes of a warp cover 128
+    // contiguous bytes of that query's dQ row
+    auto readout_dq = [&](int which) {
       ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
       fence_after_sync();
       if (__all_sync(0xffffffffu, ok)) {
-        const int q = prev_q0 + r;
-        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + (q < a.Lq ? q : 0)) * a.Hq + prev_h) * kD + 64 * cg;
+        const int qn = min(64, a.Lq - prev_q0 - 64 * cg);      // valid queries of this group
+        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + prev_q0 + 64 * cg) * a.Hq + prev_h) * kD + r;
+        const size_t qstride = static_cast<size_t>(a.Hq) * kD;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
-          if (q < a.Lq) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                         __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          for (int e = 0; e < 32; ++e) {
+            const int q = c * 32 + e;
+            if (q < qn) red_add_f32(dst + q * qstride, __uint_as_float(v[e]));
           }
         }
       }

@@ -216,14 +216,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32_sync(lane_addr + sb * 128 + c * 32, sr + c * 32);
       }
-      // row max over legal keys (raw dot products; the scale is positive)
+      // row max over legal keys (raw dot products; the scale is positive).
+      // Interior tiles (not diagonal, no ragged edge) need no masking.
       const int cmax = valid ? lim - j * kBlk : -1;
+      const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= a.Lk) && (qb + 1) * kBlk <= a.Lq;
       float mraw = -INFINITY;
+      if (interior) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float x = (c <= cmax) ? __uint_as_float(sr[c]) : -INFINITY;
-        sr[c] = __float_as_uint(x);
-        mraw = fmaxf(mraw, x);
+        for (int c = 0; c < 128; c += 2)
+          mraw = fmaxf(mraw, fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float x = (c <= cmax) ? __uint_as_float(sr[c]) : -INFINITY;
+          sr[c] = __float_as_uint(x);
+          mraw = fmaxf(mraw, x);
+        }
       }
       const float mt = mraw * a.scale_log2;
       const bool has = cmax >= 0;
