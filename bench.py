@@ -51,6 +51,23 @@ def _args():
     return p.parse_args()
 
 
+def _traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from a recorded ncu
+    capture (profiles/traffic.json), or None when there is no record or the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel, {}).get(workload)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "mass_adaptive_sparse_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -431,15 +448,24 @@ def main():
             "speedup_fwd": t_dense["fwd"] / t_main["fwd"], "speedup_bwd": t_dense["bwd"] / t_main["bwd"],
             "speedup_decode": t_dense["decode"] / t_main["decode"], "step_ms": t_dense["step"]}
 
-    # roofline of the dominant kernel: the CUDA-core kernels are bound by fp32 FMA issue
-    dom = max(("fwd", "bwd"), key=lambda p: t_main[p])
-    alu_peak = SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-    achieved = phases[dom]["tflops"]
-    roofline = {"kernel": f"mala_{dom}", "bound": "alu", "achieved": achieved, "peak": alu_peak,
-                "unit": "TFLOP/s", "frac": achieved / alu_peak, "traffic": None,
-                "peak_source": f"fp32 FMA: {SMS} SMs x 128 lanes x 2 flop x {peaks['sm_max_mhz']:.0f} MHz"}
-    decode_roof = {"achieved": phases["decode"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": phases["decode"]["gbs"] / peaks["hbm_gbs"]}
+    # roofline of every phase; the dominant one (longest) is the headline
+    roofs = {
+        "fwd": {"kernel": "fwd_tc_kernel", "bound": "tensor", "achieved": phases["fwd"]["tflops"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"},
+        "bwd": {"kernel": "bwd_tc_kernel", "bound": "tensor", "achieved": phases["bwd"]["tflops"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"},
+        "decode": {"kernel": "decode_mma_kernel", "bound": "hbm", "achieved": phases["decode"]["gbs"],
+                   "peak": peaks["hbm_gbs"], "unit": "GB/s"},
+    }
+    for ph, rf in roofs.items():
+        rf["frac"] = rf["achieved"] / rf["peak"]
+        rf["traffic"] = _traffic(rf["kernel"], pname if ph != "decode" else dname)
+        rf["peak_source"] = ("measured sustained bf16 (cuBLAS, seconds-long loop)" if rf["unit"] == "TFLOP/s"
+                             else "measured HBM copy") + f" ({peaks['source']})"
+    step_phase_ms = {"fwd": t_main["fwd"], "bwd": t_main["bwd"], "decode": t_main["decode"]}
+    dom = max(step_phase_ms, key=step_phase_ms.get)
+    roofline = dict(roofs[dom])
+    decode_roof = roofs["decode"]
 
     cpu = None
     if pool is not None:
@@ -457,7 +483,7 @@ def main():
                    f"block {dc.block} splits {dc.num_splits}", "tau": tau, "grad_dtype": "fp32",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-        "decode_roofline": decode_roof, "phases": phases, "peaks": peaks, "cpu_baseline": cpu,
+        "roofline_by_phase": roofs, "phases": phases, "peaks": peaks, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
