@@ -9,7 +9,7 @@
 // post-score work.  A retained tile runs
 //   P^T = exp(S^T - lse), dP^T = V dO^T, dS^T = P^T o (dP^T - D),
 //   dV += P^T dO, dK += dS^T Q, dQ += dS K  (formed as dQ^T = K^T dS^T and
-//   added to an fp32 accumulator).
+//   added to an fp32 accumulator by bulk tensor reduce-adds).
 //
 // All post-score products run on fp16 operands (exact fp16 copies of Q, K, V,
 // dO made by the preprocess kernel); P and dS are rounded to fp16, which keeps
@@ -59,9 +59,6 @@ struct Bars {
 };
 
 
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" :: "l"(addr), "f"(v) : "memory");
-}
 
 __device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))); }
 __device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
@@ -99,10 +96,10 @@ __device__ __forceinline__ void store_grad_row<__nv_bfloat16>(__nv_bfloat16* dst
 }
 
 template <typename Tg>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-              const BwdArgs a) {
+              const __grid_constant__ CUtensorMap mdq, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_sh;
@@ -279,28 +276,41 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     };
     if (ntiles > 0 && cg == 0) fetch(0);
 
-    // add the finished dQ^T tile (lane = head dim r, columns = queries) into the
-    // fp32 accumulator: for each query, the 32 lanes of a warp cover 128
-    // contiguous bytes of that query's dQ row
-    auto readout_dq = [&](int which) {
+    // Move the finished dQ^T tile (lane = head dim r, columns = queries) out of
+    // TMEM into registers and release the dP columns; then add it into the
+    // fp32 accumulator with two bulk reduce-adds of 64 query rows each, staged
+    // through the dS buffer (free at this point: dK and dQ have consumed it).
+    // Returns false on abort.  Thread 0 owns the bulk groups.
+    auto flush_dq = [&](int which, bool release) -> bool {
       ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
       fence_after_sync();
+      uint32_t v[64];
       if (__all_sync(0xffffffffu, ok)) {
-        const int qn = min(64, a.Lq - prev_q0 - 64 * cg);      // valid queries of this group
-        float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + prev_q0 + 64 * cg) * a.Hq + prev_h) * kD + r;
-        const size_t qstride = static_cast<size_t>(a.Hq) * kD;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int q = c * 32 + e;
-            if (q < qn) red_add_f32(dst + q * qstride, __uint_as_float(v[e]));
-          }
-        }
+        tmem_ld32_sync(lane_addr + kColDP + 64 * cg, v);
+        tmem_ld32_sync(lane_addr + kColDP + 64 * cg + 32, v + 32);
       }
       fence_before_sync();
+      if (named_vote_or(1, kMath, !ok || *abortp)) return false;
+      if (release && tid == 0) mbar_arrive(smem_u32(&bars.dq_free));
+      float* stage = reinterpret_cast<float*>(smem_raw + (sDS - smem_u32(smem_raw)));   // [64 queries][128 dims]
+#pragma unroll
+      for (int rnd = 0; rnd < 2; ++rnd) {
+        if (rnd == 1) {
+          if (tid == 0) bulk_wait_read0();
+          named_sync(1, kMath);
+        }
+        if (cg == rnd) {
+#pragma unroll
+          for (int q = 0; q < 64; ++q) stage[q * kD + r] = __uint_as_float(v[q]);
+        }
+        fence_proxy_async_smem();
+        named_sync(1, kMath);
+        if (tid == 0 && prev_q0 + 64 * rnd < a.Lq) {
+          tma_reduce_add_4d(&mdq, sDS, 0, prev_h, prev_q0 + 64 * rnd, b);
+          bulk_commit();
+        }
+      }
+      return true;
     };
 
     for (int t = 0; t < ntiles; ++t) {
@@ -415,13 +425,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         mbar_arrive(smem_u32(&bars.p_ready));
       }
       // dQ of the previous retained tile leaves the dP columns before dP^T lands there
-      if (nret > 0) {
-        readout_dq(nret - 1);
-        if (named_vote_or(1, kMath, !ok || *abortp)) break;
-        if (tid == 0) mbar_arrive(smem_u32(&bars.dq_free));
-      }
+      if (nret > 0 && !flush_dq(nret - 1, true)) break;
       ok = mbar_wait(smem_u32(&bars.dp_full), nret & 1, abortp, a.status);
       fence_after_sync();
+      // the dS buffer is free again once the bulk reduce-adds have read it
+      if (nret > 0) {
+        if (tid == 0) bulk_wait_read0();
+        named_sync(1, kMath);
+      }
       // dS^T = scale * P^T o (dP^T - D), fp16, into half cg of the swizzled dS tile (row = key r)
       if (__all_sync(0xffffffffu, ok)) {
         const float4* d4 = reinterpret_cast<const float4*>(&vec_d[vb][64 * cg]);
@@ -460,7 +471,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
 
     // last dQ tile, then dK, dV out of TMEM (loads are warp-collective; stores per key)
-    if (nret > 0 && __all_sync(0xffffffffu, ok && !*abortp)) readout_dq(nret - 1);
+    if (nret > 0 && !*abortp) flush_dq(nret - 1, false);
+    if (tid == 0) bulk_wait0();        // every reduce-add has landed before the CTA exits
     fence_after_sync();
     if (__all_sync(0xffffffffu, ok && !*abortp)) {
       const size_t off = ((static_cast<size_t>(b) * a.Lk + (key_ok ? key : 0)) * a.Hkv + hk) * kD + 64 * cg;
@@ -559,6 +571,8 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches) {
       !encode_bshd_map(&mk, k16, a.B, a.Lk, a.Hkv, kD, kBlk, true) ||
       !encode_bshd_map(&mv, v16, a.B, a.Lk, a.Hkv, kD, kBlk, true))
     return cudaErrorInvalidValue;
+  CUtensorMap mdq;
+  if (!encode_bshd_f32_map(&mdq, a.dq_acc, a.B, a.Lq, a.Hq, kD, 64)) return cudaErrorInvalidValue;
   const int tc = (a.Lk + kBlk - 1) / kBlk;
   dim3 grid(a.Hkv * a.B, tc);
   ++*launches;
@@ -566,12 +580,12 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches) {
     auto kern = bwd_tc_kernel<__nv_bfloat16>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, mdq, a);
   } else {
     auto kern = bwd_tc_kernel<float>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+    kern<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, mdo, mdq, a);
   }
   return cudaGetLastError();
 }

@@ -95,6 +95,20 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bulk tensor reduce-add of a shared-memory box into global memory, tracked
+// by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                                  int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+      :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of all committed groups may be reused
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all committed groups are complete
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -261,5 +275,7 @@ __device__ __forceinline__ int named_vote_or(int id, int count, int pred) {
 // positions beyond L read as zero.  `fp16` selects fp16 instead of bf16.
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int L, int H, int D, int box_rows,
                      bool fp16 = false);
+// Host: fp32 [B, L, H, D] tensor, box {D, 1, box_rows, 1}, no swizzle (bulk reduce-add target).
+bool encode_bshd_f32_map(CUtensorMap* map, const void* base, int B, int L, int H, int D, int box_rows);
 
 }  // namespace mala

@@ -42,4 +42,22 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int L, int H, in
   return r == CUDA_SUCCESS;
 }
 
+// fp32 [B, L, H, D] tensor (D contiguous) for bulk reduce-add of row tiles:
+// box {D, 1, box_rows, 1}, no swizzle; rows beyond L are clipped.
+bool encode_bshd_f32_map(CUtensorMap* map, const void* base, int B, int L, int H, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t e = 4;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * e, static_cast<cuuint64_t>(H) * D * e,
+                           static_cast<cuuint64_t>(L) * H * D * e};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mala
