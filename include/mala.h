@@ -209,6 +209,11 @@ mala_status mala_device_status(void* stream, int* device_code);
 /* Number of kernels this library has launched in this process (host counter). */
 uint64_t mala_launch_count(void);
 
+/* The cudaError_t behind this thread's most recent MALA_ERR_CUDA (0 if none),
+ * and its description (static string). */
+int mala_last_cuda_error(void);
+const char* mala_cuda_error_string(int code);
+
 #ifdef __cplusplus
 }
 #endif

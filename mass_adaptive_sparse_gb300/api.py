@@ -24,12 +24,13 @@ STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3:
           4: "MALA_ERR_CUDA", 5: "MALA_ERR_TIMEOUT"}
 EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bwd",
            "mala_decode_workspace_size", "mala_decode", "mala_decode_noalloc",
-           "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count")
+           "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
+           "mala_last_cuda_error", "mala_cuda_error_string")
 
 
 class MalaError(RuntimeError):
-    def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+    def __init__(self, fn: str, code: int, detail: str = ""):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}" + (f" ({detail})" if detail else ""))
         self.code = code
 
 
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.mala_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
         L.mala_launch_count.restype = ctypes.c_uint64
         L.mala_launch_count.argtypes = []
+        L.mala_last_cuda_error.restype = _i
+        L.mala_last_cuda_error.argtypes = []
+        L.mala_cuda_error_string.restype = ctypes.c_char_p
+        L.mala_cuda_error_string.argtypes = [_i]
         _lib = L
     return _lib
 
@@ -93,7 +98,11 @@ def _stream(stream):
 
 def _check(fn: str, code: int):
     if code != 0:
-        raise MalaError(fn, code)
+        detail = ""
+        if code == 4:
+            err = lib().mala_last_cuda_error()
+            detail = f"cuda error {err}: {lib().mala_cuda_error_string(err).decode()}"
+        raise MalaError(fn, code, detail)
 
 
 def _scale(d, softmax_scale):

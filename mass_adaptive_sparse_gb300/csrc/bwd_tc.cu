@@ -45,9 +45,11 @@ constexpr int kTile = kBlk * kD * 2;    // 32 KiB of fp16
 constexpr int kHalf = kTile / 2;
 constexpr int kThreads = 320;
 constexpr int kMath = 256;            // two math warpgroups
-// shared memory: K, V, Q[2], dO, dS
-constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile;
-constexpr int kSmem = 6 * kTile + 1024;
+// shared memory: K, V, Q[2], dO, dS (doubles as dQ staging for queries 0-63),
+// dQ staging for queries 64-127
+constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile,
+              kOffST = 6 * kTile;
+constexpr int kSmem = 7 * kTile + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 struct Bars {
@@ -96,7 +98,7 @@ __device__ __forceinline__ void store_grad_row<__nv_bfloat16>(__nv_bfloat16* dst
 }
 
 template <typename Tg>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
               const __grid_constant__ CUtensorMap mdq, const BwdArgs a) {
@@ -105,10 +107,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   __shared__ uint32_t tmem_sh;
   __shared__ int flag;
   __shared__ int abort_flag;
-  __shared__ __align__(16) float vec_lse[2][kBlk], vec_d[2][kBlk], vec_c[2][kBlk];
+  __shared__ __align__(16) float vec_lse[kBlk], vec_d[kBlk], vec_c[kBlk];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO, sDS = base + kOffDS;
+  const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO, sDS = base + kOffDS,
+                 sST = base + kOffST;
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int bh = blockIdx.x;
@@ -277,38 +280,31 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (ntiles > 0 && cg == 0) fetch(0);
 
     // Move the finished dQ^T tile (lane = head dim r, columns = queries) out of
-    // TMEM into registers and release the dP columns; then add it into the
-    // fp32 accumulator with two bulk reduce-adds of 64 query rows each, staged
-    // through the dS buffer (free at this point: dK and dQ have consumed it).
-    // Returns false on abort.  Thread 0 owns the bulk groups.
+    // TMEM, release the dP columns, and add it into the fp32 accumulator with
+    // two bulk reduce-adds of 64 query rows: group 0 stages its rows in the dS
+    // buffer (free: dK and dQ have consumed it), group 1 in the staging buffer.
+    // Thread 0 owns the bulk groups.  Returns false on abort.
     auto flush_dq = [&](int which, bool release) -> bool {
       ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
       fence_after_sync();
-      uint32_t v[64];
+      float* stage = reinterpret_cast<float*>(smem_raw + ((cg == 0 ? sDS : sST) - smem_u32(smem_raw)));
       if (__all_sync(0xffffffffu, ok)) {
-        tmem_ld32_sync(lane_addr + kColDP + 64 * cg, v);
-        tmem_ld32_sync(lane_addr + kColDP + 64 * cg + 32, v + 32);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * kD + r] = __uint_as_float(v[e]);
+        }
       }
       fence_before_sync();
+      fence_proxy_async_smem();
       if (named_vote_or(1, kMath, !ok || *abortp)) return false;
-      if (release && tid == 0) mbar_arrive(smem_u32(&bars.dq_free));
-      float* stage = reinterpret_cast<float*>(smem_raw + (sDS - smem_u32(smem_raw)));   // [64 queries][128 dims]
-#pragma unroll
-      for (int rnd = 0; rnd < 2; ++rnd) {
-        if (rnd == 1) {
-          if (tid == 0) bulk_wait_read0();
-          named_sync(1, kMath);
-        }
-        if (cg == rnd) {
-#pragma unroll
-          for (int q = 0; q < 64; ++q) stage[q * kD + r] = __uint_as_float(v[q]);
-        }
-        fence_proxy_async_smem();
-        named_sync(1, kMath);
-        if (tid == 0 && prev_q0 + 64 * rnd < a.Lq) {
-          tma_reduce_add_4d(&mdq, sDS, 0, prev_h, prev_q0 + 64 * rnd, b);
-          bulk_commit();
-        }
+      if (tid == 0) {
+        if (release) mbar_arrive(smem_u32(&bars.dq_free));
+        if (prev_q0 < a.Lq) tma_reduce_add_4d(&mdq, sDS, 0, prev_h, prev_q0, b);
+        if (prev_q0 + 64 < a.Lq) tma_reduce_add_4d(&mdq, sST, 0, prev_h, prev_q0 + 64, b);
+        bulk_commit();
       }
       return true;
     };
@@ -316,11 +312,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     for (int t = 0; t < ntiles; ++t) {
       const int h = hk * G + t / ni, i = ibot + t % ni;
       const int q0 = i * kBlk;
-      const int vb = t & 1;
       if (cg == 0) {
-        vec_lse[vb][r] = n_lse;
-        vec_d[vb][r] = n_d;
-        vec_c[vb][r] = n_c;
+        vec_lse[r] = n_lse;
+        vec_d[r] = n_d;
+        vec_c[r] = n_c;
       }
       named_sync(1, kMath);
       if (cg == 0 && t + 1 < ntiles) fetch(t + 1);
@@ -332,7 +327,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int qlim = a.Lq - q0;                 // query columns at or beyond this are out of range
       const int qmin = diag ? r : 0;              // causal: query >= key inside the diagonal tile
       const bool interior = !diag && qlim >= kBlk && keys_full;
-      const float4* c4 = reinterpret_cast<const float4*>(&vec_c[vb][64 * cg]);
+      const float4* c4 = reinterpret_cast<const float4*>(&vec_c[64 * cg]);
       int keep_row = 0;
       if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
@@ -351,7 +346,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int q = 64 * cg + c * 32 + e;
-              if (key_ok && q < qlim && q >= qmin) gap = fmaxf(gap, __uint_as_float(sr[e]) - vec_c[vb][q]);
+              if (key_ok && q < qlim && q >= qmin) gap = fmaxf(gap, __uint_as_float(sr[e]) - vec_c[q]);
             }
           }
           keep_row |= gap >= 0.f ? 1 : 0;
@@ -389,7 +384,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
       }
       // P^T = exp2(S * scale_log2 - lse) in fp16, written over this group's S columns
-      const float4* l4 = reinterpret_cast<const float4*>(&vec_lse[vb][64 * cg]);
+      const float4* l4 = reinterpret_cast<const float4*>(&vec_lse[64 * cg]);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -410,8 +405,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const int q = 64 * cg + c * 32 + e;
             const bool l0 = key_ok && q < qlim && q >= qmin;
             const bool l1 = key_ok && q + 1 < qlim && q + 1 >= qmin;
-            const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -vec_lse[vb][q])) : 0.f;
-            const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -vec_lse[vb][q + 1])) : 0.f;
+            const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -vec_lse[q])) : 0.f;
+            const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -vec_lse[q + 1])) : 0.f;
             pk[c * 16 + e / 2] = pack_f16(p0, p1);
           }
         }
@@ -435,7 +430,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       // dS^T = scale * P^T o (dP^T - D), fp16, into half cg of the swizzled dS tile (row = key r)
       if (__all_sync(0xffffffffu, ok)) {
-        const float4* d4 = reinterpret_cast<const float4*>(&vec_d[vb][64 * cg]);
+        const float4* d4 = reinterpret_cast<const float4*>(&vec_d[64 * cg]);
         const float sc = a.scale;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {

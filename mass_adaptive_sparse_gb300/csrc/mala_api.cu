@@ -18,6 +18,7 @@ using namespace mala;
 __device__ int g_device_status = 0;
 
 std::atomic<uint64_t> g_launches{0};
+thread_local int g_last_cuda_error = 0;   // cudaError_t of this thread's last MALA_ERR_CUDA
 
 constexpr int kMaxDevices = 64;
 
@@ -39,6 +40,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 mala_status finish(cudaError_t e, int launches) {
   g_launches.fetch_add(static_cast<uint64_t>(launches), std::memory_order_relaxed);
+  if (e != cudaSuccess) g_last_cuda_error = static_cast<int>(e);
   return e == cudaSuccess ? MALA_OK : MALA_ERR_CUDA;
 }
 
@@ -291,5 +293,9 @@ mala_status mala_device_status(void* stream, int* device_code) {
 }
 
 uint64_t mala_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mala_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* mala_cuda_error_string(int code) { return cudaGetErrorString(static_cast<cudaError_t>(code)); }
 
 }  // extern "C"
