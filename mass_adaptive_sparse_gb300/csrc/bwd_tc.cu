@@ -423,12 +423,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (nret > 0 && !flush_dq(nret - 1, true)) break;
       ok = mbar_wait(smem_u32(&bars.dp_full), nret & 1, abortp, a.status);
       fence_after_sync();
-      // the dS buffer is free again once the bulk reduce-adds have read it
-      if (nret > 0) {
-        if (tid == 0) bulk_wait_read0();
-        named_sync(1, kMath);
-      }
-      // dS^T = scale * P^T o (dP^T - D), fp16, into half cg of the swizzled dS tile (row = key r)
+      // dS^T = scale * P^T o (dP^T - D), fp16, computed into registers first so
+      // that the bulk reduce-adds have time to finish reading the dS buffer
+      uint32_t w[32];
       if (__all_sync(0xffffffffu, ok)) {
         const float4* d4 = reinterpret_cast<const float4*>(&vec_d[64 * cg]);
         const float sc = a.scale;
@@ -436,25 +433,29 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         for (int c = 0; c < 2; ++c) {
           uint32_t dp[32];
           tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, dp);
-          uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const float4 dd = d4[(c * 32 + 2 * e) / 4];
             const uint32_t pw0 = pk[c * 16 + e], pw1 = pk[c * 16 + e + 1];
-            w[e] = pack_f16(sc * f16_lo(pw0) * (__uint_as_float(dp[2 * e]) - dd.x),
-                            sc * f16_hi(pw0) * (__uint_as_float(dp[2 * e + 1]) - dd.y));
-            w[e + 1] = pack_f16(sc * f16_lo(pw1) * (__uint_as_float(dp[2 * e + 2]) - dd.z),
-                                sc * f16_hi(pw1) * (__uint_as_float(dp[2 * e + 3]) - dd.w));
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = c * 4 + u;                 // 16-byte chunk (8 queries) inside the 128-byte row
-            const uint32_t addr = sDS + cg * kHalf + r * 128 + ((chunk ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                         :: "r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
-                         : "memory");
+            w[c * 16 + e] = pack_f16(sc * f16_lo(pw0) * (__uint_as_float(dp[2 * e]) - dd.x),
+                                     sc * f16_hi(pw0) * (__uint_as_float(dp[2 * e + 1]) - dd.y));
+            w[c * 16 + e + 1] = pack_f16(sc * f16_lo(pw1) * (__uint_as_float(dp[2 * e + 2]) - dd.z),
+                                         sc * f16_hi(pw1) * (__uint_as_float(dp[2 * e + 3]) - dd.w));
           }
         }
+      }
+      // the dS buffer is free again once the bulk reduce-adds have read it
+      if (nret > 0) {
+        if (tid == 0) bulk_wait_read0();
+        named_sync(1, kMath);
+      }
+      // into half cg of the swizzled dS tile (row = key r): 8 chunks of 8 queries
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t addr = sDS + cg * kHalf + r * 128 + ((u ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(addr), "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                     : "memory");
       }
       fence_proxy_async_smem();
       fence_before_sync();
