@@ -286,6 +286,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // Thread 0 owns the bulk groups.  Returns false on abort.
     auto flush_dq = [&](int which, bool release) -> bool {
       ok = ok && mbar_wait(smem_u32(&bars.dq_full), which & 1, abortp, a.status);
+      // the staging buffer of group 1 was last read by the previous flush's second reduce-add
+      if (tid == 0) bulk_wait_read0();
+      named_sync(1, kMath);
       fence_after_sync();
       float* stage = reinterpret_cast<float*>(smem_raw + ((cg == 0 ? sDS : sST) - smem_u32(smem_raw)));
       if (__all_sync(0xffffffffu, ok)) {
@@ -302,7 +305,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (named_vote_or(1, kMath, !ok || *abortp)) return false;
       if (tid == 0) {
         if (release) mbar_arrive(smem_u32(&bars.dq_free));
+        // two bulk groups: the first (staged in the dS buffer) is waited for alone before dS is written
         if (prev_q0 < a.Lq) tma_reduce_add_4d(&mdq, sDS, 0, prev_h, prev_q0, b);
+        bulk_commit();
         if (prev_q0 + 64 < a.Lq) tma_reduce_add_4d(&mdq, sST, 0, prev_h, prev_q0 + 64, b);
         bulk_commit();
       }
@@ -444,9 +449,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           }
         }
       }
-      // the dS buffer is free again once the bulk reduce-adds have read it
+      // the dS buffer is free again once the first bulk reduce-add has read it
       if (nret > 0) {
-        if (tid == 0) bulk_wait_read0();
+        if (tid == 0) bulk_wait_read1();
         named_sync(1, kMath);
       }
       // into half cg of the swizzled dS tile (row = key r): 8 chunks of 8 queries
