@@ -7,13 +7,15 @@
 // rowmax(S) - m - log l < log(tau / L_q) (l = 0 keeps).  A skipped tile issues
 // no V load and no P V product and leaves (m, l, O) unchanged (App. A.1).
 //
-// One CTA = one query block of one head, 192 threads:
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r.  Reads S from
-//              TMEM, takes the row max, votes on the tile, and for retained
-//              tiles issues the V load (thread 0), computes P = exp2(S - m) in
-//              bf16 into TMEM (over S's columns) and updates l.
-//   warp 4     TMA producer for Q and K (3-stage K ring).
-//   warp 5     MMA issuer: S = Q K^T (SS, K-major operands) and
+// One CTA = one query block of one head, 320 threads:
+//   warps 0-7  softmax, two warpgroups: thread (c, r) owns columns [64c, 64c+64)
+//              of query row r = TMEM lane r.  The groups combine the row max
+//              and row sums through shared memory (each keeps a copy of the
+//              row state), vote on the tile, and for retained tiles thread 0
+//              issues the V load; P = exp2(S - m) goes as bf16 into TMEM
+//              inside each group's own S columns.
+//   warp 8     TMA producer for Q and K (2-stage K ring).
+//   warp 9     MMA issuer: S = Q K^T (SS, K-major operands) and
 //              O += P V (A = P from TMEM, B = V MN-major), accumulate in TMEM.
 // TMEM: three S buffers (columns 0, 128, 256) and O (columns 384..511), so
 // scores run two tiles ahead of the softmax while a retained tile waits for
@@ -34,10 +36,11 @@ constexpr int kD = 128;                 // head dim
 constexpr int kBlk = 128;               // B_q = B_k
 constexpr int kTile = kBlk * kD * 2;    // 32 KiB: one 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;        // one 64-column TMA box
-constexpr int kNK = 3;                  // K stages
+constexpr int kNK = 2;                  // K stages
 constexpr int kNV = 3;                  // V stages
 constexpr int kNS = 3;                  // S buffers in TMEM
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoft = 256;              // two softmax warpgroups
 constexpr int kSmem = kTile * (1 + kNK + kNV) + 1024;
 constexpr uint32_t kColO = 384;
 constexpr float kRescale = 8.0f;        // move the running max only past 2^8 growth
@@ -85,6 +88,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   __shared__ uint32_t tmem_sh;
   __shared__ int flag[kNS];
   __shared__ int abort_flag;
+  __shared__ float xmax[2][kBlk], xsum[2][kBlk], xsumr[2][kBlk];   // per-group row partials
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base;
@@ -118,7 +122,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t tmem = tmem_sh;
   volatile int* abortp = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer: Q once, then the K ring ----------------
     if (lane == 0) {
       prefetch_tensormap(&mq);
@@ -143,7 +147,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       for (int t = max(0, issued - kNK); t < issued; ++t)
         mbar_wait(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, abortp, a.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(1, 0, 0, kBlk, kBlk);
@@ -177,11 +181,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           if (!mbar_wait(smem_u32(&bars.v_full[vs]), (npv / kNV) & 1, abortp, a.status)) break;
           fence_after_sync();
           const uint32_t vbase = sV + vs * kTile;
+          // P: keys 0-63 packed in columns 0-31 of the S buffer, keys 64-127 in 64-95
           const uint32_t p_tmem = tmem + sb * 128;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColO, p_tmem + k * 8, desc_mnmajor_sw128(vbase + k * 2048, kHalf, 1024), idesc_pv,
-                   (npv > 0 || k > 0) ? 1u : 0u);
+            mma_ts(tmem + kColO, p_tmem + (k / 4) * 64 + (k % 4) * 8, desc_mnmajor_sw128(vbase + k * 2048, kHalf, 1024),
+                   idesc_pv, (npv > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars.v_empty[vs]));
           mma_commit(smem_u32(&bars.pv_done[npv & 1]));
           ++npv;
@@ -192,16 +197,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_wait(smem_u32(&bars.fin), 0, abortp, a.status);
     }
   } else {
-    // ---------------- softmax: thread r = query row r = TMEM lane r ----------------
-    const int r = tid;
+    // ---------------- softmax: thread (cg, r) = columns [64cg, 64cg+64) of row r ----------------
+    const int r = tid & 127, cg = tid >> 7;
     const int qrow = qb * kBlk + r;
     const bool valid = qrow < a.Lq;
     const int lim = a.causal ? min(qrow, a.Lk - 1) : a.Lk - 1;   // last legal key of this row
     const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk));
     const bool test = a.tau > 0.f;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // l: exact fp32 sum of P (Eq. 3 test and lse); lr: sum of the bf16-rounded P
-    // that enters the P V product (normalises O consistently with it)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    // row state, identical in both groups: l is the exact fp32 sum of P (Eq. 3
+    // test and lse); lr sums the bf16-rounded P that enters the P V product
     float m_used = -INFINITY, l = 0.f, lr = 0.f;
     int nret = 0, vissued = 0;
     bool ok = true;
@@ -211,43 +216,45 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int j = jtop - t, sb = t % kNS;
       ok = mbar_wait(smem_u32(&bars.s_full[sb]), (t / kNS) & 1, abortp, a.status);
       fence_after_sync();
-      uint32_t sr[128];                       // raw scores Q.K (fp32 bits), later packed P
+      uint32_t sr[64];                        // raw scores Q.K of this group's columns, later packed P
       if (__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_sync(lane_addr + sb * 128 + c * 32, sr + c * 32);
+        tmem_ld32_sync(lane_addr + sb * 128 + 64 * cg, sr);
+        tmem_ld32_sync(lane_addr + sb * 128 + 64 * cg + 32, sr + 32);
       }
       // row max over legal keys (raw dot products; the scale is positive).
       // Interior tiles (not diagonal, no ragged edge) need no masking.
-      const int cmax = valid ? lim - j * kBlk : -1;
+      const int cmax = valid ? lim - j * kBlk - 64 * cg : -1;
       const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= a.Lk) && (qb + 1) * kBlk <= a.Lq;
       float mraw = -INFINITY;
       if (interior) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 2)
+        for (int c = 0; c < 64; c += 2)
           mraw = fmaxf(mraw, fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])));
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float x = (c <= cmax) ? __uint_as_float(sr[c]) : -INFINITY;
           sr[c] = __float_as_uint(x);
           mraw = fmaxf(mraw, x);
         }
       }
-      const float mt = mraw * a.scale_log2;
-      const bool has = cmax >= 0;
+      xmax[cg][r] = mraw;
+      named_sync(1, kSoft);
+      const float mt = fmaxf(xmax[0][r], xmax[1][r]) * a.scale_log2;
+      const bool has = valid && lim >= j * kBlk;
       const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
       fence_before_sync();
-      const int keep = named_vote_or(1, 128, keep_row);
-      if (named_vote_or(1, 128, !ok || *abortp)) break;
+      const int keep = named_vote_or(1, kSoft, keep_row);
+      if (named_vote_or(1, kSoft, !ok || *abortp)) break;
       if (!keep) {
-        if (r == 0) {
+        if (tid == 0) {
           flag[sb] = 0;
           mbar_arrive(smem_u32(&bars.sm_done[sb]));
           if (mask_row) mask_row[j] = 0;
         }
         continue;
       }
-      if (r == 0) {
+      if (tid == 0) {
         // V of this tile: loaded only now that the tile is retained
         const int vs = vissued % kNV, n = vissued / kNV;
         if (n > 0) ok = mbar_wait(smem_u32(&bars.v_empty[vs]), (n - 1) & 1, abortp, a.status);
@@ -270,7 +277,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const float nscale = a.scale_log2;
       float rowsum = 0.f, rowsum_r = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), nscale, -mref));
         const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), nscale, -mref));
         const uint32_t w = pack_bf16(p0, p1);
@@ -278,8 +285,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         rowsum_r += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         sr[c] = w;                            // P packed over the consumed scores
       }
-      l = l * alpha + rowsum;
-      lr = lr * alpha + rowsum_r;
+      xsum[cg][r] = rowsum;
+      xsumr[cg][r] = rowsum_r;
       // O must be rescaled when the reference max moved: wait for the last P V
       if (nret > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const int prev = nret - 1;
@@ -287,21 +294,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         fence_after_sync();
         if (__all_sync(0xffffffffu, ok)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32_sync(lane_addr + kColO + c * 32, o);
+            tmem_ld32_sync(lane_addr + kColO + 64 * cg + c * 32, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_addr + kColO + c * 32, o);
+            tmem_st32(lane_addr + kColO + 64 * cg + c * 32, o);
           }
         }
       }
-      tmem_st32(lane_addr + sb * 128, sr);
-      tmem_st32(lane_addr + sb * 128 + 32, sr + 32);
+      tmem_st32(lane_addr + sb * 128 + 64 * cg, sr);   // inside this group's own S columns
       tmem_st_wait();
       fence_before_sync();
-      if (named_vote_or(1, 128, !ok || *abortp)) break;
-      if (r == 0) {
+      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also publishes xsum / xsumr
+      l = l * alpha + (xsum[0][r] + xsum[1][r]);
+      lr = lr * alpha + (xsumr[0][r] + xsumr[1][r]);
+      if (tid == 0) {
         flag[sb] = 1;
         mbar_arrive(smem_u32(&bars.sm_done[sb]));
       }
@@ -318,16 +326,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
       const float inv = 1.f / lr;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32_sync(lane_addr + kColO + c * 32, reinterpret_cast<uint32_t*>(o));
-        if (valid) store_row<Tout>(orow + c * 32, o, inv);
+        tmem_ld32_sync(lane_addr + kColO + 64 * cg + c * 32, reinterpret_cast<uint32_t*>(o));
+        if (valid) store_row<Tout>(orow + 64 * cg + c * 32, o, inv);
       }
-      if (valid) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m_used + log2f(l)) * kLn2;
-      if (a.counts != nullptr && r == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = nret;
+      if (valid && cg == 0) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m_used + log2f(l)) * kLn2;
+      if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = nret;
     }
     // V loads issued but never consumed (abort path) must land before exit
-    if (r == 0) {
+    if (tid == 0) {
       for (int n = max(0, vissued - kNV); n < vissued; ++n)
         mbar_wait(smem_u32(&bars.v_full[n % kNV]), (n / kNV) & 1, abortp, a.status);
     }
