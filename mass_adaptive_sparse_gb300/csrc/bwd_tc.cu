@@ -202,6 +202,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const uint32_t qb = sQ + (t & 1) * kTile;
         if (ret) {
           if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status)) break;
+          fence_after_sync();
+          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
+          // queries 64-127 in columns 64-95, each written by its math group).
+          // Issued before dP so that the next tile's scores can follow at once.
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
+                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
+        }
+        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
+        if (ret) {
           if (nret > 0 && !mbar_wait(smem_u32(&bars.dq_free), (nret - 1) & 1, abortp, a.status)) break;
           fence_after_sync();
           // dP^T = V dO^T
@@ -211,15 +222,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mma_ss(tmem + kColDP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
           }
           mma_commit(smem_u32(&bars.dp_full));
-          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
-          // queries 64-127 in columns 64-95, each written by its math group)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
-                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars.do_empty));
         }
-        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
         if (!ret) {
           mma_commit(smem_u32(&bars.q_empty[t & 1]));
           continue;
@@ -269,7 +273,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (q < a.Lq) {
         const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.Lq + q;
         n_lse = a.lse[off] * kLog2e;
-        n_d = a.delta[off];
+        n_d = a.delta[off] * a.scale;          // scale * D: dS = P (scale dP - scale D)
         const float thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
                                : -INFINITY;
         n_c = (n_lse + thr) * inv_sl2;
@@ -442,10 +446,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           for (int e = 0; e < 16; e += 2) {
             const float4 dd = d4[(c * 32 + 2 * e) / 4];
             const uint32_t pw0 = pk[c * 16 + e], pw1 = pk[c * 16 + e + 1];
-            w[c * 16 + e] = pack_f16(sc * f16_lo(pw0) * (__uint_as_float(dp[2 * e]) - dd.x),
-                                     sc * f16_hi(pw0) * (__uint_as_float(dp[2 * e + 1]) - dd.y));
-            w[c * 16 + e + 1] = pack_f16(sc * f16_lo(pw1) * (__uint_as_float(dp[2 * e + 2]) - dd.z),
-                                         sc * f16_hi(pw1) * (__uint_as_float(dp[2 * e + 3]) - dd.w));
+            w[c * 16 + e] = pack_f16(f16_lo(pw0) * fmaf(sc, __uint_as_float(dp[2 * e]), -dd.x),
+                                     f16_hi(pw0) * fmaf(sc, __uint_as_float(dp[2 * e + 1]), -dd.y));
+            w[c * 16 + e + 1] = pack_f16(f16_lo(pw1) * fmaf(sc, __uint_as_float(dp[2 * e + 2]), -dd.z),
+                                         f16_hi(pw1) * fmaf(sc, __uint_as_float(dp[2 * e + 3]), -dd.w));
           }
         }
       }
