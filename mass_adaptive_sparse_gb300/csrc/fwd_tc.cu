@@ -217,10 +217,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.s_full[sb]), (t / kNS) & 1, abortp, a.status);
       fence_after_sync();
       uint32_t sr[64];                        // raw scores Q.K of this group's columns, later packed P
-      if (__all_sync(0xffffffffu, ok)) {
-        tmem_ld32_sync(lane_addr + sb * 128 + 64 * cg, sr);
-        tmem_ld32_sync(lane_addr + sb * 128 + 64 * cg + 32, sr + 32);
-      }
+      if (__all_sync(0xffffffffu, ok)) tmem_ld64_sync(lane_addr + sb * 128 + 64 * cg, sr);
       // row max over legal keys (raw dot products; the scale is positive).
       // Interior tiles (not diagonal, no ragged edge) need no masking.
       const int cmax = valid ? lim - j * kBlk - 64 * cg : -1;

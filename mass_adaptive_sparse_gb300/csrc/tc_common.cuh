@@ -178,6 +178,23 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
       : "r"(taddr) : "memory");
 }
 
+#define MALA_R8B(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                    "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+// Load 64 consecutive 32-bit columns of this thread's TMEM lane in one
+// instruction and wait for them.
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, "
+      "%35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, "
+      "%56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MALA_R8B(0), MALA_R8B(8), MALA_R8B(16), MALA_R8B(24), MALA_R8B(32), MALA_R8B(40), MALA_R8B(48),
+        MALA_R8B(56)
+      : "r"(taddr) : "memory");
+}
+#undef MALA_R8B
+
 // Store 32 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
