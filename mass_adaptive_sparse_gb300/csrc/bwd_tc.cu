@@ -296,10 +296,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       fence_after_sync();
       float* stage = reinterpret_cast<float*>(smem_raw + ((cg == 0 ? sDS : sST) - smem_u32(smem_raw)));
       if (__all_sync(0xffffffffu, ok)) {
-        uint32_t v[64];
-        tmem_ld64_sync(lane_addr + kColDP + 64 * cg, v);
 #pragma unroll
-        for (int e = 0; e < 64; ++e) stage[e * kD + r] = __uint_as_float(v[e]);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * kD + r] = __uint_as_float(v[e]);
+        }
       }
       fence_before_sync();
       fence_proxy_async_smem();
@@ -336,11 +339,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const float4* c4 = reinterpret_cast<const float4*>(&vec_c[64 * cg]);
       int keep_row = 0;
       if (__all_sync(0xffffffffu, ok)) {
-        uint32_t sall[64];
-        tmem_ld64_sync(lane_addr + kColS + 64 * cg, sall);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t* sr = sall + c * 32;
+          uint32_t sr[32];
+          tmem_ld32_sync(lane_addr + kColS + 64 * cg + c * 32, sr);
           float gap = -INFINITY;
           if (interior) {
 #pragma unroll
@@ -436,11 +438,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (__all_sync(0xffffffffu, ok)) {
         const float4* d4 = reinterpret_cast<const float4*>(&vec_d[64 * cg]);
         const float sc = a.scale;
-        uint32_t dpall[64];
-        tmem_ld64_sync(lane_addr + kColDP + 64 * cg, dpall);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t* dp = dpall + c * 32;
+          uint32_t dp[32];
+          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, dp);
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const float4 dd = d4[(c * 32 + 2 * e) / 4];
