@@ -9,14 +9,16 @@
 // is kept if any of them keeps it.  The split writes (m, l, l_rounded, u) for
 // the exact merge of "Why exact attention does not need a quadratic matrix".
 //
-// One CTA of 160 threads per (split, KV head, sequence):
-//   warp 4     TMA producer: K tiles, 3-stage ring, running ahead.
-//   warps 0-3  S^T = K q^T with mma.sync m16n8k16 (keys as M, the G <= 8 heads
-//              as N), row max per head, vote; for kept tiles thread 0 issues
-//              the V load, P (bf16) goes to a shared slot, and the P V product
-//              O^T += V^T P^T (warp w owns head dims 32w..32w+31) runs up to two
-//              kept tiles later, so each V load has two tiles of work to land.
-// The reference max m is moved lazily (only past 2^8 growth); every pending P
+// One CTA of 288 threads per (KV head, split, sequence):
+//   warp 8     TMA producer: K tiles, 3-stage ring, running ahead.
+//   warps 0-3  score warps: S^T = K q^T with mma.sync m16n8k16 (keys as M, the
+//              G <= 8 heads as N), one barrier per tile that exchanges each
+//              warp's tile maxima and running partial sums, the test (lane g
+//              decides head g, a ballot combines the heads), and for kept
+//              tiles the V load and P (bf16) into one of three slots.
+//   warps 4-7  P V warps: O^T += V^T P^T for each published slot (warp w owns
+//              head dims 32(w-4)..32(w-4)+31), off the score warps' path.
+// The reference max m is moved lazily (only past 2^8 growth); every P slot
 // carries the m it was computed with, and O is rescaled to it before its P V.
 #include <cuda_bf16.h>
 
@@ -33,14 +35,14 @@ constexpr int kBK = 128;
 constexpr int kTile = kBK * kD * 2;
 constexpr int kHalf = kTile / 2;
 constexpr int kNK = 3;          // K ring
-constexpr int kNV = 3;          // V ring = pending P slots
-constexpr int kThreads = 160;
+constexpr int kNV = 3;          // V ring = P slots
+constexpr int kThreads = 288;
 constexpr int kSmem = kTile * (kNK + kNV) + 1024;
 constexpr float kRescale = 8.0f;
 
 struct Bars {
   uint64_t k_full[kNK], k_empty[kNK];
-  uint64_t v_full[kNV];
+  uint64_t v_full[kNV], p_full[kNV], slot_empty[kNV];
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -68,19 +70,27 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int row, int dchunk) 
   return base + (dchunk >> 3) * kHalf + row * 128 + (((dchunk & 7) ^ (row & 7)) << 4);
 }
 
+__device__ __forceinline__ float* split_record(const DecArgs& a, int sp, int b, int h) {
+  return a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + h) * (kD + 4);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const DecArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ int abort_flag;
-  __shared__ float red_max[2][4][8], red_sum[4][8], red_sumr[4][8];   // red_max double-buffered by tile
-  __shared__ __align__(16) uint16_t pslot[kNV][8][kBK];   // P (bf16) of pending kept tiles, [head][key]
+  __shared__ int pv_done;                                   // P V products finished (for the exit path)
+  // per score warp: tile max and running partial sums (exact, rounded) per head; by tile parity
+  // (index 2 of xl: the final sums, written while a slower warp may still read index 0 or 1)
+  __shared__ float xmax[2][4][8], xl[3][4][8], xlr[4][8];
+  __shared__ __align__(16) uint16_t pslot[kNV][8][kBK];    // P (bf16) of kept tiles, [head][key]
   __shared__ float pslot_m[kNV][8];                         // reference max each P was taken against
+  __shared__ int pslot_end[kNV];                            // 1: no more tiles
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sK = base, sV = base + kNK * kTile;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int sp = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int hk = blockIdx.x, sp = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
   const int T = (a.N + kBK - 1) / kBK;
   const int per = (T + a.splits - 1) / a.splits;
@@ -89,14 +99,19 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
 
   if (tid == 0) {
     abort_flag = 0;
+    pv_done = 0;
     for (int i = 0; i < kNK; ++i) { mbar_init(smem_u32(&bars.k_full[i]), 1); mbar_init(smem_u32(&bars.k_empty[i]), 1); }
-    for (int i = 0; i < kNV; ++i) mbar_init(smem_u32(&bars.v_full[i]), 1);
+    for (int i = 0; i < kNV; ++i) {
+      mbar_init(smem_u32(&bars.v_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_full[i]), 128);
+      mbar_init(smem_u32(&bars.slot_empty[i]), 128);
+    }
     fence_barrier_init();
   }
   __syncthreads();
   volatile int* abortp = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0 && ntiles > 0) {
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
@@ -111,17 +126,77 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
         tma_load_4d(sK + s * kTile + kHalf, &mk, kf, 64, hk, row, b);
         ++issued;
       }
+      int never = 0;      // in-flight K loads must land before exit, abort or not
       for (int t = max(0, issued - kNK); t < issued; ++t)
-        mbar_wait(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, abortp, a.status);
+        mbar_wait(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, &never, a.status);
     }
     return;
   }
 
-  // ---------------- compute warps ----------------
+  const int gq = lane >> 2, cq = lane & 3;       // fragment row group / column pair
+
+  if (warp >= 4) {
+    // ---------------- P V warps ----------------
+    const int pw = warp - 4;
+    float m_o0 = -INFINITY, m_o1 = -INFINITY;   // reference max of this thread's O columns (heads 2cq, 2cq+1)
+    float o[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+    bool ok = true;
+    int n = 0;
+    for (;; ++n) {
+      const int vs = n % kNV;
+      ok = ok && mbar_wait(smem_u32(&bars.p_full[vs]), (n / kNV) & 1, abortp, a.status);
+      if (!__all_sync(0xffffffffu, ok) || pslot_end[vs]) break;
+      ok = ok && mbar_wait(smem_u32(&bars.v_full[vs]), (n / kNV) & 1, abortp, a.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // rescale O to the reference max this P was taken against
+      const float mn0 = pslot_m[vs][2 * cq], mn1 = pslot_m[vs][2 * cq + 1];
+      const float f0 = (m_o0 == -INFINITY) ? 0.f : ex2(m_o0 - mn0);
+      const float f1 = (m_o1 == -INFINITY) ? 0.f : ex2(m_o1 - mn1);
+      if (mn0 != -INFINITY) { o[0][0] *= f0; o[0][2] *= f0; o[1][0] *= f0; o[1][2] *= f0; m_o0 = mn0; }
+      if (mn1 != -INFINITY) { o[0][1] *= f1; o[0][3] *= f1; o[1][1] *= f1; o[1][3] *= f1; m_o1 = mn1; }
+      const uint32_t vbase = sV + vs * kTile;
+      const uint32_t* prow = reinterpret_cast<const uint32_t*>(&pslot[vs][gq][0]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t b0 = prow[(16 * k + 2 * cq) / 2];
+        const uint32_t b1 = prow[(16 * k + 8 + 2 * cq) / 2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          // A = V^T (16 d x 16 keys): four 8x8 transposed loads
+          const int key = 16 * k + (lane & 7) + 8 * (lane >> 4);
+          const int dchunk = (32 * pw + 16 * mt) / 8 + ((lane >> 3) & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(sw_addr(vbase, key, dchunk), a0, a1, a2, a3);
+          mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      mbar_arrive(smem_u32(&bars.slot_empty[vs]));
+    }
+    if (tid == 128) pv_done = n;
+    if (__all_sync(0xffffffffu, ok) && !*abortp) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hrow = 0; hrow < 2; ++hrow) {
+          const int d = 32 * pw + 16 * mt + gq + 8 * hrow;
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (2 * cq + e < G) split_record(a, sp, b, hk * G + 2 * cq + e)[4 + d] = o[mt][2 * hrow + e];
+        }
+    }
+    named_sync(2, 256);
+    return;
+  }
+
+  // ---------------- score warps ----------------
   const bool test = a.tau > 0.f;
   const float thr = a.log2_tau - log2f(static_cast<float>(a.N));
   const float sl2 = a.scale_log2;
-  const int gq = lane >> 2, cq = lane & 3;       // fragment row group / column pair
+  const int g = lane & 7;                        // the head this lane decides
 
   // q^T as the B operand (K = d, N = heads): b0b1 = q[head gq][16k + 2cq ..], b2b3 = q[gq][16k + 8 + 2cq ..]
   uint32_t qb[8][2];
@@ -134,47 +209,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
       qb[k][1] = gq < G ? qrow[(16 * k + 8 + 2 * cq) / 2] : 0u;
     }
   }
-  float m_ref[8], l_ex[8], l_rd[8];
-#pragma unroll
-  for (int g = 0; g < 8; ++g) { m_ref[g] = -INFINITY; l_ex[g] = 0.f; l_rd[g] = 0.f; }
-  float m_o0 = -INFINITY, m_o1 = -INFINITY;   // reference max of this thread's O columns (heads 2cq, 2cq+1)
-  float o[2][4];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
-  int nret = 0, npv = 0, kept = 0;
+  float m_g = -INFINITY;                 // reference max of head g
+  float lw0 = 0.f, lw1 = 0.f;            // this warp's partial sums for heads 2cq, 2cq+1 (exact)
+  float lr0 = 0.f, lr1 = 0.f;            // the same sums of P as rounded to bf16
+  int nret = 0, kept = 0;
   bool ok = true;
-
-  // O^T += V^T P^T for the pending kept tile number n
-  auto pv = [&](int n) {
-    const int vs = n % kNV;
-    ok = ok && mbar_wait(smem_u32(&bars.v_full[vs]), (n / kNV) & 1, abortp, a.status);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    // rescale O to the reference max this P was taken against
-    const float mn0 = pslot_m[vs][(2 * cq) & 7], mn1 = pslot_m[vs][(2 * cq + 1) & 7];
-    const float f0 = (m_o0 == -INFINITY) ? 0.f : ex2(m_o0 - mn0);
-    const float f1 = (m_o1 == -INFINITY) ? 0.f : ex2(m_o1 - mn1);
-    if (mn0 != -INFINITY) { o[0][0] *= f0; o[0][2] *= f0; o[1][0] *= f0; o[1][2] *= f0; m_o0 = mn0; }
-    if (mn1 != -INFINITY) { o[0][1] *= f1; o[0][3] *= f1; o[1][1] *= f1; o[1][3] *= f1; m_o1 = mn1; }
-    const uint32_t vbase = sV + vs * kTile;
-    const uint32_t* prow = reinterpret_cast<const uint32_t*>(&pslot[vs][gq][0]);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t b0 = prow[(16 * k + 2 * cq) / 2];
-      const uint32_t b1 = prow[(16 * k + 8 + 2 * cq) / 2];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        // A = V^T (16 d x 16 keys): four 8x8 transposed loads
-        const int key = 16 * k + (lane & 7) + 8 * (lane >> 4);
-        const int dchunk = (32 * warp + 16 * mt) / 8 + ((lane >> 3) & 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(sw_addr(vbase, key, dchunk), a0, a1, a2, a3);
-        mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
-      }
-    }
-    ++npv;
-  };
 
   for (int t = 0; t < ntiles; ++t) {
     const int j = t1 - 1 - t;
@@ -219,116 +258,101 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    if (gq == 0) { red_max[t & 1][warp][2 * cq] = mx0; red_max[t & 1][warp][2 * cq + 1] = mx1; }
-    if (named_vote_or(1, 128, !ok || *abortp)) break;      // also the barrier for red_max / K reads
+    // publish this tile's maxima and the partial sums after the previous tile
+    if (gq == 0) {
+      xmax[t & 1][warp][2 * cq] = mx0; xmax[t & 1][warp][2 * cq + 1] = mx1;
+      xl[t & 1][warp][2 * cq] = lw0; xl[t & 1][warp][2 * cq + 1] = lw1;
+    }
+    if (named_vote_or(1, 128, !ok || *abortp)) break;      // also the barrier for the exchange / K reads
     if (tid == 0) mbar_arrive(smem_u32(&bars.k_empty[s]));
-    float mt_h[8];
-    int keep = !test;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      mt_h[g] = fmaxf(fmaxf(red_max[t & 1][0][g], red_max[t & 1][1][g]), fmaxf(red_max[t & 1][2][g], red_max[t & 1][3][g]));
-      if (g < G && test && (l_ex[g] == 0.f || !(mt_h[g] - m_ref[g] - lg2(l_ex[g]) < thr))) keep = 1;
-    }
+    // Eq. (3) for head g: tile max - (m + log2 l) < log2(tau / N), l = 0 keeps
+    const float tm = fmaxf(fmaxf(xmax[t & 1][0][g], xmax[t & 1][1][g]), fmaxf(xmax[t & 1][2][g], xmax[t & 1][3][g]));
+    const float lt = (xl[t & 1][0][g] + xl[t & 1][1][g]) + (xl[t & 1][2][g] + xl[t & 1][3][g]);
+    const bool keep_g = g < G && (lt == 0.f || !(tm - m_g - lg2(lt) < thr));
+    const bool keep = !test || __any_sync(0xffffffffu, keep_g);
     if (a.mask != nullptr && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * T + j] = keep ? 1 : 0;
-    if (keep) {
-      ++kept;
-      const int vs = nret % kNV;
-      if (tid == 0) {
-        // V of this tile: loaded only now that the tile is kept; its slot was
-        // freed by the P V of kept tile nret - kNV, finished before the barrier above
-        const uint32_t vf = smem_u32(&bars.v_full[vs]);
-        mbar_expect_tx(vf, kTile);
-        tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBK, b);
-        tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBK, b);
-      }
-      // lazily moved reference max, then P = exp2(s - m) as bf16 into the slot
-      float alpha[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        alpha[g] = 1.f;
-        if (mt_h[g] > m_ref[g] + kRescale) {
-          alpha[g] = (m_ref[g] == -INFINITY) ? 0.f : ex2(m_ref[g] - mt_h[g]);
-          m_ref[g] = mt_h[g];
-        }
-      }
-      const float mr0 = m_ref[2 * cq] == -INFINITY ? 0.f : m_ref[2 * cq];
-      const float mr1 = m_ref[2 * cq + 1] == -INFINITY ? 0.f : m_ref[2 * cq + 1];
-      float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int hrow = 0; hrow < 2; ++hrow) {
-          const int key = 32 * warp + 16 * mt + gq + 8 * hrow;
-          const float p0 = ex2(acc[mt][2 * hrow] - mr0);
-          const float p1 = ex2(acc[mt][2 * hrow + 1] - mr1);
-          const uint32_t w = pack_bf16(p0, p1);
-          se0 += p0; se1 += p1;
-          sr0 += __uint_as_float(w << 16);
-          sr1 += __uint_as_float(w & 0xffff0000u);
-          if (2 * cq < 8) pslot[vs][2 * cq][key] = static_cast<uint16_t>(w & 0xffffu);
-          if (2 * cq + 1 < 8) pslot[vs][2 * cq + 1][key] = static_cast<uint16_t>(w >> 16);
-        }
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        se0 += __shfl_xor_sync(0xffffffffu, se0, off);
-        se1 += __shfl_xor_sync(0xffffffffu, se1, off);
-        sr0 += __shfl_xor_sync(0xffffffffu, sr0, off);
-        sr1 += __shfl_xor_sync(0xffffffffu, sr1, off);
-      }
-      if (gq == 0) {
-        red_sum[warp][2 * cq] = se0; red_sum[warp][2 * cq + 1] = se1;
-        red_sumr[warp][2 * cq] = sr0; red_sumr[warp][2 * cq + 1] = sr1;
-      }
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        if (tid == g) pslot_m[vs][g] = m_ref[g];
-      named_sync(1, 128);
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        l_ex[g] = l_ex[g] * alpha[g] + (red_sum[0][g] + red_sum[1][g] + red_sum[2][g] + red_sum[3][g]);
-        l_rd[g] = l_rd[g] * alpha[g] + (red_sumr[0][g] + red_sumr[1][g] + red_sumr[2][g] + red_sumr[3][g]);
-      }
-      ++nret;
-      // keep at most kNV - 1 products pending; the oldest runs now
-      if (nret - npv >= kNV) pv(npv);
-      named_sync(1, 128);        // red_sum reads done before the next tile overwrites them
+    if (!keep) continue;
+    ++kept;
+    const int vs = nret % kNV;
+    // the slot (P and V) is free once the P V of kept tile nret - kNV is done
+    if (nret >= kNV) ok = ok && mbar_wait(smem_u32(&bars.slot_empty[vs]), ((nret / kNV) - 1) & 1, abortp, a.status);
+    if (!__all_sync(0xffffffffu, ok)) continue;        // the next tile's vote ends every score warp's loop
+    if (tid == 96) {
+      const uint32_t vf = smem_u32(&bars.v_full[vs]);
+      mbar_expect_tx(vf, kTile);
+      tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBK, b);
+      tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBK, b);
     }
-  }
-  while (npv < nret && __all_sync(0xffffffffu, ok) && !*abortp) pv(npv);
-
-  // split record: (m, l, l_rounded, 0, u[D]) per query head, m in log2 units
-  if (__all_sync(0xffffffffu, ok && !*abortp)) {
+    // lazily moved reference max (lane g), broadcast for this thread's heads 2cq, 2cq+1
+    float alpha_g = 1.f;
+    if (tm > m_g + kRescale) {
+      alpha_g = (m_g == -INFINITY) ? 0.f : ex2(m_g - tm);
+      m_g = tm;
+    }
+    const float m0 = __shfl_sync(0xffffffffu, m_g, 2 * cq), m1 = __shfl_sync(0xffffffffu, m_g, 2 * cq + 1);
+    const float al0 = __shfl_sync(0xffffffffu, alpha_g, 2 * cq), al1 = __shfl_sync(0xffffffffu, alpha_g, 2 * cq + 1);
+    const float mr0 = m0 == -INFINITY ? 0.f : m0;
+    const float mr1 = m1 == -INFINITY ? 0.f : m1;
+    float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
-        const int d = 32 * warp + 16 * mt + gq + 8 * hrow;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int g = 2 * cq + e;
-          if (g < G) {
-            float* rec = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (kD + 4);
-            rec[4 + d] = o[mt][2 * hrow + e];
-          }
-        }
+        const int key = 32 * warp + 16 * mt + gq + 8 * hrow;
+        const float p0 = ex2(acc[mt][2 * hrow] - mr0);
+        const float p1 = ex2(acc[mt][2 * hrow + 1] - mr1);
+        const uint32_t w = pack_bf16(p0, p1);
+        se0 += p0; se1 += p1;
+        sr0 += __uint_as_float(w << 16);
+        sr1 += __uint_as_float(w & 0xffff0000u);
+        pslot[vs][2 * cq][key] = static_cast<uint16_t>(w & 0xffffu);
+        pslot[vs][2 * cq + 1][key] = static_cast<uint16_t>(w >> 16);
       }
     }
+    if (warp == 0 && lane < 8) pslot_m[vs][lane] = m_g;
+    if (tid == 0) pslot_end[vs] = 0;
+    mbar_arrive(smem_u32(&bars.p_full[vs]));
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      if (tid == g && g < G) {
-        float* rec = a.partial + ((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + g) * (kD + 4);
-        rec[0] = m_ref[g];
-        rec[1] = l_ex[g];
-        rec[2] = l_rd[g];
-        rec[3] = 0.f;
-      }
+    for (int off = 4; off < 32; off <<= 1) {
+      se0 += __shfl_xor_sync(0xffffffffu, se0, off);
+      se1 += __shfl_xor_sync(0xffffffffu, se1, off);
+      sr0 += __shfl_xor_sync(0xffffffffu, sr0, off);
+      sr1 += __shfl_xor_sync(0xffffffffu, sr1, off);
     }
-    if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+    lw0 = lw0 * al0 + se0; lw1 = lw1 * al1 + se1;
+    lr0 = lr0 * al0 + sr0; lr1 = lr1 * al1 + sr1;
+    ++nret;
   }
-  // V loads issued but never consumed (abort path) must land before exit
-  if (tid == 0)
-    for (int n = npv; n < nret; ++n) mbar_wait(smem_u32(&bars.v_full[n % kNV]), (n / kNV) & 1, abortp, a.status);
+  // end of tiles for the P V warps (their slot must be free first)
+  const int es = nret % kNV;
+  if (nret >= kNV) ok = ok && mbar_wait(smem_u32(&bars.slot_empty[es]), ((nret / kNV) - 1) & 1, abortp, a.status);
+  if (ok) {
+    if (tid == 0) pslot_end[es] = 1;
+    mbar_arrive(smem_u32(&bars.p_full[es]));
+  }
+
+  // split record: (m, l, l_rounded, 0) per query head, m in log2 units
+  if (gq == 0) {
+    xl[2][warp][2 * cq] = lw0; xl[2][warp][2 * cq + 1] = lw1;
+    xlr[warp][2 * cq] = lr0; xlr[warp][2 * cq + 1] = lr1;
+  }
+  named_sync(1, 128);
+  if (warp == 0 && lane < G && !*abortp) {
+    float* rec = split_record(a, sp, b, hk * G + lane);
+    rec[0] = m_g;
+    rec[1] = (xl[2][0][lane] + xl[2][1][lane]) + (xl[2][2][lane] + xl[2][3][lane]);
+    rec[2] = (xlr[0][lane] + xlr[1][lane]) + (xlr[2][lane] + xlr[3][lane]);
+    rec[3] = 0.f;
+  }
+  if (a.counts != nullptr && tid == 0 && !*abortp)
+    a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+  named_sync(2, 256);
+  // V loads issued but never consumed (abort path) must land before exit; these
+  // waits ignore the abort flag (they are still bounded in time)
+  if (tid == 0) {
+    int never = 0;
+    for (int n = pv_done; n < nret; ++n) mbar_wait(smem_u32(&bars.v_full[n % kNV]), (n / kNV) & 1, &never, a.status);
+  }
 }
 
 }  // namespace
@@ -343,7 +367,7 @@ cudaError_t launch_decode_mma(const DecArgs& a, cudaStream_t s, int* launches) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.splits, a.Hkv, a.B);
+  dim3 grid(a.Hkv, a.splits, a.B);
   ++*launches;
   decode_mma_kernel<<<grid, kThreads, kSmem, s>>>(mk, mv, a);
   return cudaGetLastError();
