@@ -202,28 +202,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const uint32_t qb = sQ + (t & 1) * kTile;
         if (ret) {
           if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status)) break;
-          fence_after_sync();
-          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
-          // queries 64-127 in columns 64-95, each written by its math group).
-          // Issued before dP so that the next tile's scores can follow at once.
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
-                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
-        }
-        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
-        if (ret) {
+          // dQ of the previous retained tile has left the dP columns
           if (nret > 0 && !mbar_wait(smem_u32(&bars.dq_free), (nret - 1) & 1, abortp, a.status)) break;
           fence_after_sync();
-          // dP^T = V dO^T
+          // dP^T = V dO^T first: the math warps' dS work then overlaps dV and the next scores
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
             mma_ss(tmem + kColDP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
           }
           mma_commit(smem_u32(&bars.dp_full));
+          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
+          // queries 64-127 in columns 64-95, each written by its math group)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
+                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars.do_empty));
         }
+        // the next scores overwrite P^T, which dV (issued above, executed in order) has read
+        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
         if (!ret) {
           mma_commit(smem_u32(&bars.q_empty[t & 1]));
           continue;
@@ -264,21 +262,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     bool ok = true;
     int prev_q0 = 0, prev_h = 0;   // query block / head of the last retained tile (for the dQ read-out)
 
-    // per-query vectors of tile t (fetched by group 0): lse (log2 units), D,
-    // and the decision threshold in raw dot units (keep iff raw S >= c)
-    float n_lse = 0.f, n_d = 0.f, n_c = 0.f;
+    // per-query vectors of tile t (fetched by group 0 one tile ahead): lse and
+    // D as loaded, and the decision threshold log2(tau / L_q).  The arithmetic
+    // on the loaded values waits until the vectors are written, a tile later,
+    // so the loads' latency is not paid where they are issued.
+    float n_lse = 0.f, n_d = 0.f, n_thr = INFINITY;
     auto fetch = [&](int t) {
       const int h = hk * G + t / ni, i = ibot + t % ni;
       const int q = i * kBlk + r;
       if (q < a.Lq) {
         const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.Lq + q;
-        n_lse = a.lse[off] * kLog2e;
-        n_d = a.delta[off] * a.scale;          // scale * D: dS = P (scale dP - scale D)
-        const float thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
-                               : -INFINITY;
-        n_c = (n_lse + thr) * inv_sl2;
+        n_lse = a.lse[off];
+        n_d = a.delta[off];
+        n_thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
+                     : -INFINITY;
       } else {
-        n_lse = 0.f; n_d = 0.f; n_c = INFINITY;
+        n_lse = 0.f; n_d = 0.f; n_thr = INFINITY;     // out of range: never kept
       }
     };
     if (ntiles > 0 && cg == 0) fetch(0);
@@ -322,9 +321,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int h = hk * G + t / ni, i = ibot + t % ni;
       const int q0 = i * kBlk;
       if (cg == 0) {
-        vec_lse[r] = n_lse;
-        vec_d[r] = n_d;
-        vec_c[r] = n_c;
+        // lse in log2 units; scale * D (dS = P (scale dP - scale D)); the
+        // threshold on the raw dot product (keep iff raw S >= c)
+        const float l2 = n_lse * kLog2e;
+        vec_lse[r] = l2;
+        vec_d[r] = n_d * a.scale;
+        vec_c[r] = n_thr == INFINITY ? INFINITY : (l2 + n_thr) * inv_sl2;
       }
       named_sync(1, kMath);
       if (cg == 0 && t + 1 < ntiles) fetch(t + 1);
