@@ -210,18 +210,19 @@ def _worker_init():
     os.environ["OMP_NUM_THREADS"] = "1"
 
 
-def oracle_sample(workload, pool, cores, rank_seed=0):
+def oracle_sample(workload, pool, cores, rank_seed=0, rounds=1):
     """Times the oracle on a bounded sample and extrapolates to one full step.
-    Sample: forward + the matching backward dQ column for `cores` query blocks
-    of head 0 of the prefill workload (spread over the sequence), and `cores`
-    (sequence 0, KV head) groups of the decode workload."""
+    Sample: forward + the matching backward dQ column for `rounds * cores`
+    query blocks of head 0 of the prefill workload (spread over the
+    sequence), and up to `rounds * cores` (sequence, KV head) groups of the
+    decode workload."""
     from mass_adaptive_sparse_gb300 import synthetic
     pname, dname = WORKLOADS[workload]
     pc, dc = synthetic.CONFIGS[pname], synthetic.CONFIGS[dname]
     tr = pc.L // pc.block
-    nblk = max(2, cores)
-    blocks = [int(round((tr - 1) * (s + 1) / nblk)) for s in range(nblk)]
-    groups = [g % dc.Hkv for g in range(max(1, min(cores, dc.Hkv)))]
+    nblk = min(tr, max(2, cores * rounds))
+    blocks = sorted({int(round((tr - 1) * (s + 1) / nblk)) for s in range(nblk)})
+    groups = list(range(max(1, min(cores * rounds, dc.B * dc.Hkv))))
     tasks = [("prefill", pname, pc.seed + rank_seed, i) for i in blocks]
     tasks += [("decode", dname, dc.seed + rank_seed, g) for g in groups]
     t0 = time.perf_counter()
@@ -236,8 +237,9 @@ def oracle_sample(workload, pool, cores, rank_seed=0):
     full_groups = dc.B * dc.Hkv
     # per-unit CPU seconds x full units, spread over `cores` workers
     step_s = (pre_cpu / pre_tiles * full_tiles + dec_cpu / len(dec) * full_groups) / cores
-    sample = (f"fp64 oracle: forward + backward dQ column of query blocks {blocks} (head 0, "
-              f"{pre_tiles} tiles each way) of {pname} and decode of {len(dec)} (sequence 0, KV head) "
+    shown = blocks if len(blocks) <= 16 else f"{len(blocks)} evenly spaced from {blocks[0]} to {blocks[-1]}"
+    sample = (f"fp64 oracle: forward + backward dQ column of query blocks {shown} (head 0, "
+              f"{pre_tiles} tiles each way) of {pname} and decode of {len(dec)} (sequence, KV head) "
               f"groups of {dname}; extrapolated by tiles ({full_tiles}) and groups ({full_groups})")
     return step_s * 1e3, wall, sample
 
@@ -469,7 +471,10 @@ def main():
 
     cpu = None
     if pool is not None:
-        val, wall, sample = oracle_sample(args.workload, pool, cores)
+        # a short calibration round, then a sample of about --sample-seconds
+        _, wall1, _ = oracle_sample(args.workload, pool, cores)
+        rounds = max(1, int(round(args.sample_seconds / max(wall1, 1e-3))))
+        val, wall, sample = oracle_sample(args.workload, pool, cores, rounds=rounds)
         cpu = {"value": val, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample,
                "sample_wall_s": wall}
         pool.close()
