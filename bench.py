@@ -6,7 +6,9 @@ One step = one pass of the whole path on synthetic planted-peak data:
   heads, L=131072, d=128, bf16, 128x128 tiles) and one split-KV decode step on
   the 128K decode workload (batch 8, 32 query / 8 KV heads, 131072-token bf16
   cache, 16 splits), all at tau = 1.
-The same steps are then timed at tau = 0 (dense, same kernels) for the speedup.
+The same steps are then timed at tau = 0 (dense, same kernels) for the speedup,
+and the 32K prefill workload's forward and backward are timed at both taus
+(reported under "secondary").
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
@@ -47,6 +49,7 @@ def _args():
     p.add_argument("--no-dense", action="store_true", help="skip the tau = 0 comparison loop")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-32k", action="store_true", help="skip the 32K prefill timing (128k workload)")
     p.add_argument("--sample-seconds", type=float, default=15.0)
     return p.parse_args()
 
@@ -469,6 +472,59 @@ def main():
     roofline = dict(roofs[dom])
     decode_roof = roofs["decode"]
 
+    # --- the metric's second length: 32K prefill, fwd + bwd at tau and at 0 ---
+    # (its tensors fit in L2, so L2 is flushed before every timed launch)
+    secondary = None
+    if args.workload == "128k" and not args.no_32k:
+        c32 = synthetic.CONFIGS["prefill_32k"]
+        x32 = synthetic.prefill_inputs(c32, seed=c32.seed + rank)
+        e = {n: x32[n].to(dev) for n in ("q", "k", "v", "do")}
+        del x32
+        B3, L3, H3, _ = e["q"].shape
+        e["o"] = torch.empty_like(e["q"])
+        e["lse"] = torch.empty((B3, H3, L3), dtype=torch.float32, device=dev)
+        for n, like in (("dq", "q"), ("dk", "k"), ("dv", "v")):
+            e[n] = torch.empty(e[like].shape, dtype=torch.float32, device=dev)
+        e["ws"] = torch.empty(max(256, api.mala_bwd_workspace_size(e["q"], e["k"], torch.float32)),
+                              dtype=torch.uint8, device=dev)
+        tr3 = -(-L3 // c32.block)
+        cf3 = torch.zeros((B3, H3, tr3), dtype=torch.int32, device=dev)
+        cb3 = torch.zeros((B3, H3, tr3), dtype=torch.int32, device=dev)
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+        def f32k(t):
+            api.mala_fwd(e["q"], e["k"], e["v"], e["o"], e["lse"], block=c32.block, tau=t, retained_counts=cf3)
+
+        def b32k(t):
+            api.mala_bwd(e["q"], e["k"], e["v"], e["o"], e["do"], e["lse"], e["dq"], e["dk"], e["dv"], e["ws"],
+                         block=c32.block, tau=t, retained_counts=cb3)
+
+        def time32(t):
+            for _ in range(max(3, args.warmup)):
+                f32k(t); b32k(t)
+            barrier()
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+            for s_ in range(args.steps):
+                flush.zero_()
+                ev[s_][0].record(stream); f32k(t); ev[s_][1].record(stream)
+                flush.zero_()
+                ev[s_][2].record(stream); b32k(t); ev[s_][3].record(stream)
+            barrier()
+            return (max_over_ranks(statistics.mean(x[0].elapsed_time(x[1]) for x in ev)),
+                    max_over_ranks(statistics.mean(x[2].elapsed_time(x[3]) for x in ev)))
+
+        f1, b1 = time32(tau)
+        kf3, kb3 = int(cf3.sum().item()), int(cb3.sum().item())
+        f0, b0 = time32(0.0)
+        u3 = prefill_units(c32)
+        secondary = {"prefill_32k": {
+            "shape": f"B={B3} H={H3}/{e['k'].shape[2]} L={L3} d={c32.d} tiles {c32.block}x{c32.block}",
+            "l2": "flushed before every timed launch",
+            "fwd": {"ms": f1, "tflops": fwd_flops(c32, kf3) / f1 / 1e9, "kept_fraction": kf3 / u3["legal_tiles"]},
+            "bwd": {"ms": b1, "tflops": bwd_flops(c32, kb3) / b1 / 1e9, "kept_fraction": kb3 / u3["legal_tiles"]},
+            "dense": {"fwd_ms": f0, "bwd_ms": b0, "speedup_fwd": f0 / f1, "speedup_bwd": b0 / b1}}}
+        del e, flush
+
     cpu = None
     if pool is not None:
         # a short calibration round, then a sample of about --sample-seconds
@@ -488,7 +544,8 @@ def main():
                    f"block {dc.block} splits {dc.num_splits}", "tau": tau, "grad_dtype": "fp32",
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-        "roofline_by_phase": roofs, "phases": phases, "peaks": peaks, "cpu_baseline": cpu,
+        "roofline_by_phase": roofs, "phases": phases, "secondary": secondary, "peaks": peaks,
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

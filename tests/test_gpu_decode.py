@@ -1,4 +1,5 @@
 """GPU parity of mala_decode (split-KV decode + exact merge) against the oracle."""
+import dataclasses
 import math
 
 import numpy as np
@@ -73,6 +74,19 @@ def test_decode_small_bf16(splits, tau):
 def test_decode_small_fp32_d64(block):
     cfg = synthetic.CONFIGS["decode_128k"]
     _check(cfg, 777, 2, 1.0, 5, block, 12, dtype=torch.float32, d=64)
+
+
+@pytest.mark.parametrize("H,Hkv", [(16, 2), (8, 4), (4, 4)])
+def test_decode_group_sizes(H, Hkv):
+    """Query-head groups of 8, 2 and 1 (the tensor-core kernel takes up to 8)."""
+    cfg = dataclasses.replace(synthetic.CONFIGS["decode_128k"], H=H, Hkv=Hkv)
+    _check(cfg, 1500, 2, 1.0, 4, 128, 41)
+
+
+def test_decode_single_partial_tile():
+    """A cache shorter than one tile: one ragged tile, every other split empty."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 77, 2, 1.0, 16, 128, 53)
 
 
 def test_decode_tau0_is_dense_for_any_split():

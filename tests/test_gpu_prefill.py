@@ -1,7 +1,8 @@
 """GPU parity of mala_fwd / mala_bwd against the fp64 oracle, through the C ABI.
 
 Small cases are compared element by element (several tiles, ragged tails,
-GQA, tau in {0, 1, 4, 1e30}); the 8K, 32K and 128K workloads run at full size
+GQA, batch 2, non-causal with Lq != Lk, bf16 gradients, fp32 output from bf16
+inputs, tau in {0, 1, 4, 64, 1e30}); the 8K, 32K and 128K workloads run at full size
 in the launch configuration the benchmark times and are compared on sampled
 heads and query / key blocks, which the oracle computes exactly.
 """
@@ -20,12 +21,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _inputs(cfg, L=None, seed=None, heads=None, hkv=None):
-    x = synthetic.prefill_inputs(cfg, L=L, seed=seed)
+def _inputs(cfg, L=None, seed=None, heads=None, hkv=None, lk=None):
+    """The recipe's q, k, v, dO; `lk` (non-causal cases) keeps the first L query
+    rows and the first lk key rows of a sequence as long as the longer of them."""
+    x = synthetic.prefill_inputs(cfg, L=L if lk is None else max(L, lk), seed=seed)
     q, k, v, do = x["q"], x["k"], x["v"], x["do"]
     if heads is not None:
         q, do = q[:, :, :heads].contiguous(), do[:, :, :heads].contiguous()
         k, v = k[:, :, :hkv].contiguous(), v[:, :, :hkv].contiguous()
+    if lk is not None:
+        q, do = q[:, :L].contiguous(), do[:, :L].contiguous()
+        k, v = k[:, :lk].contiguous(), v[:, :lk].contiguous()
     return q, k, v, do
 
 
@@ -48,30 +54,32 @@ def _oracle_bwd_inputs(ref_fwd, gpu_o, gpu_lse, heads, blocks, block, dtype):
 
 
 def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, grad=True,
-              q_blocks=None, dq_blocks=None, dk_blocks=None, ref_heads=None):
+              q_blocks=None, dq_blocks=None, dk_blocks=None, ref_heads=None, causal=True, lk=None,
+              grad_dtype=torch.float32, out_dtype=None):
     block = block or cfg.block
-    q, k, v, do = _inputs(cfg, L=L, seed=seed, heads=heads, hkv=hkv)
+    q, k, v, do = _inputs(cfg, L=L, seed=seed, heads=heads, hkv=hkv, lk=lk)
     fp32 = (q.dtype == torch.float32) if fp32 is None else fp32
     d = q.shape[3]
     scale = 1.0 / math.sqrt(d)
     qd, kd, vd, dod = _gpu(q, k, v, do)
-    o, lse, info = api.forward(qd, kd, vd, tau, block=block, counts=True, mask=True)
+    o, lse, info = api.forward(qd, kd, vd, tau, causal=causal, block=block, out_dtype=out_dtype,
+                               counts=True, mask=True)
     torch.cuda.synchronize()
     assert api.mala_device_status() == 0
     q64, k64, v64, do64 = (parity.to64(t) for t in (q, k, v, do))
     H = q.shape[2]
     ref_heads = list(range(H)) if ref_heads is None else ref_heads
-    tr = -(-L // block)
+    tr, tc = -(-L // block), -(-k.shape[1] // block)
     fwd_blocks = q_blocks if q_blocks is not None else list(range(tr))
     if dq_blocks is not None:
         fwd_blocks = sorted(set(fwd_blocks) | set(dq_blocks) | {i for i in range(tr) if i >= min(dk_blocks)})
-    ref = orc.mala_forward_bshd(q64, k64, v64, scale, tau, block, block, heads=ref_heads,
+    ref = orc.mala_forward_bshd(q64, k64, v64, scale, tau, block, block, causal=causal, heads=ref_heads,
                                 query_blocks=fwd_blocks)
     gpu_o, gpu_lse, gpu_mask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
-    metrics = parity.check_forward(gpu_o, gpu_lse, gpu_mask, ref, q64, k64, v64, scale, block, q.dtype,
-                                   fp32, heads=ref_heads, blocks=q_blocks)
+    metrics = parity.check_forward(gpu_o, gpu_lse, gpu_mask, ref, q64, k64, v64, scale, block, o.dtype,
+                                   fp32, heads=ref_heads, causal=causal, blocks=q_blocks)
     counts = info["counts"].cpu().numpy()
-    legal_gpu = np.tril(np.ones((tr, tr), bool))
+    legal_gpu = np.tril(np.ones((tr, tc), bool)) if causal else np.ones((tr, tc), bool)
     np.testing.assert_array_equal(counts, (gpu_mask.astype(bool) & legal_gpu).sum(-1))
     if not grad:
         return metrics
@@ -81,12 +89,13 @@ def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, gr
     else:
         o_in, lse_in = _oracle_bwd_inputs(ref, o, lse, ref_heads, fwd_blocks, block, q.dtype)
         tiles = lambda i, j: i in dq_blocks or j in dk_blocks
-    dq, dk, dv, binfo = api.backward(qd, kd, vd, o_in, dod, lse_in, tau, block=block, counts=True, mask=True)
+    dq, dk, dv, binfo = api.backward(qd, kd, vd, o_in, dod, lse_in, tau, causal=causal, block=block,
+                                     grad_dtype=grad_dtype, counts=True, mask=True)
     torch.cuda.synchronize()
     assert api.mala_device_status() == 0
     o_in64, lse_in64 = parity.to64(o_in), parity.to64(lse_in)
     refb = orc.mala_backward_bshd(q64, k64, v64, o_in64, do64, lse_in64, scale, tau, block, block,
-                                  heads=ref_heads, tiles=tiles)
+                                  causal=causal, heads=ref_heads, tiles=tiles)
     gpu_b = {"dq": parity.to64(dq), "dk": parity.to64(dk), "dv": parity.to64(dv),
              "mask": binfo["mask"].cpu().numpy()}
     # compare only the sampled heads (and KV heads whose every query head is sampled)
@@ -112,11 +121,11 @@ def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, gr
         if h not in ref_heads:
             sel_legal[:, h] = False
     refb_cmp = dict(refb, legal=sel_legal)
-    bm = parity.check_backward(gpu_b, refb_cmp, block, fp32, dq_rows=dq_rows, dk_rows=dk_rows)
+    bm = parity.check_backward(gpu_b, refb_cmp, block, fp32, dq_rows=dq_rows, dk_rows=dk_rows,
+                               grad_dtype=grad_dtype)
     # backward support is nested in the forward support on oracle-fed rows (MALA §2.2)
     assert not (refb["retained"] & ~ref["retained"] & sel_legal).any()
-    tc = -(-k.shape[1] // block)
-    np.testing.assert_array_equal(binfo["counts"].cpu().numpy(), (gmask.astype(bool) & legal_gpu[:, :tc]).sum(-2))
+    np.testing.assert_array_equal(binfo["counts"].cpu().numpy(), (gmask.astype(bool) & legal_gpu).sum(-2))
     metrics["bwd"] = bm
     return metrics
 
@@ -145,6 +154,34 @@ def test_bf16_small_cases(block, L, tau):
 def test_bf16_gqa_small():
     cfg = synthetic.PrefillConfig("gqa", 1, 4, 2, 600, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.01)
     _run_case(cfg, 600, 1.0, 23, block=128)
+
+
+def test_bf16_batch2_gqa():
+    """Two sequences, 8 query heads over 2 KV heads (group 4), ragged length."""
+    cfg = synthetic.PrefillConfig("b2gqa", 2, 8, 2, 700, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.01)
+    _run_case(cfg, 700, 1.0, 43, block=128)
+
+
+@pytest.mark.parametrize("L,lk", [(300, 700), (640, 256)])
+@pytest.mark.parametrize("tau", [1.0, 64.0])
+def test_bf16_noncausal(L, lk, tau):
+    """causal = 0: every key visible to every query, L_q = Lk, Lq != Lk."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run_case(cfg, L, tau, 37, heads=2, hkv=2, block=128, causal=False, lk=lk)
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.0])
+def test_bf16_gradients_in_bf16(tau):
+    """grad dtype bf16: the fp32 dQ accumulator in the workspace, then a
+    conversion; compared with the oracle rounded to bf16."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run_case(cfg, 600, tau, 31, heads=2, hkv=2, block=128, grad_dtype=torch.bfloat16)
+
+
+def test_fp32_output_from_bf16_inputs():
+    """out dtype fp32 for bf16 q, k, v (forward only: the backward takes O in the input dtype)."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run_case(cfg, 1000, 1.0, 47, heads=2, hkv=2, block=128, out_dtype=torch.float32, grad=False)
 
 
 def test_fp32_d128_block64():
