@@ -48,8 +48,13 @@ def is_borderline(margin) -> np.ndarray:
         return np.isfinite(m) & (np.abs(np.expm1(m)) <= orc.BORDERLINE_REL)
 
 
-def check_close(name, got, ref, out_dtype, ref_round=True, fp32=False):
-    """Assert the tolerance of the output dtype; returns the metrics."""
+FP16_UNIT_ROUNDOFF = 2.0 ** -11
+
+
+def check_close(name, got, ref, out_dtype, ref_round=True, fp32=False, abs_floor_rel=0.0):
+    """Assert the tolerance of the output dtype; returns the metrics.
+    ``abs_floor_rel`` > 0 raises the bf16 max-abs bound to
+    max(BF16_MAX_ABS, abs_floor_rel * max|ref|)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
@@ -61,7 +66,8 @@ def check_close(name, got, ref, out_dtype, ref_round=True, fp32=False):
         return {"max_abs": float(err.max())}
     rref = round_like(ref, out_dtype) if (ref_round and out_dtype == torch.bfloat16) else ref
     mean_rel = float(np.abs(got - rref).sum() / max(np.abs(rref).sum(), 1e-30))
-    assert err.max() <= BF16_MAX_ABS, f"{name}: max abs err {err.max():.3g} > {BF16_MAX_ABS}"
+    lim = max(BF16_MAX_ABS, abs_floor_rel * float(np.abs(ref).max()))
+    assert err.max() <= lim, f"{name}: max abs err {err.max():.3g} > {lim:.3g}"
     assert mean_rel <= BF16_MEAN_REL, f"{name}: mean rel err {mean_rel:.3g} > {BF16_MEAN_REL}"
     return {"max_abs": float(err.max()), "mean_rel": mean_rel}
 
@@ -152,7 +158,12 @@ def check_forward(gpu_o, gpu_lse, gpu_mask, ref, q, k, v, scale, block, out_dtyp
 def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=True, grad_dtype=torch.float32):
     """gpu / ref: dicts with dq, dk, dv (numpy, BSHD) and mask / retained,
     legal, margin ([B, H, Tr, Tc]).  ``dq_rows`` / ``dk_rows`` restrict the
-    comparison to boolean masks [B, L, H] / [B, L, Hkv] (sampled checks)."""
+    comparison to boolean masks [B, L, H] / [B, L, Hkv] (sampled checks).
+
+    With grouped query heads, dK and dV sum over the group, so they grow with
+    it while their error stays near fp16's unit roundoff relative to the
+    largest value (the post-score products take fp16 operands): their max-abs
+    bound is max(2e-2, 2^-11 max|ref|).  Without groups the bound is 2e-2."""
     B, Lq, H, D = gpu["dq"].shape
     Lk, Hkv = gpu["dk"].shape[1], gpu["dk"].shape[2]
     grp = H // Hkv
@@ -173,6 +184,7 @@ def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=Tru
         if grad_dtype == torch.bfloat16:
             metrics[name] = check_close_bf16_rounded(name, gpu[name][ok], ref[name][ok])
         else:
+            floor = FP16_UNIT_ROUNDOFF if (grp > 1 and name != "dq") else 0.0
             metrics[name] = check_close(name, gpu[name][ok], ref[name][ok], torch.float32, ref_round=False,
-                                        fp32=fp32)
+                                        fp32=fp32, abs_floor_rel=floor)
     return metrics
