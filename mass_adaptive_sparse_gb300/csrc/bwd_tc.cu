@@ -21,9 +21,12 @@
 // queries); warp 8 = TMA producer (K, V once; Q ring); warp 9 =
 // MMA issuer.  dS is stored pre-multiplied by the softmax scale, so dQ and dK
 // come out of the products already scaled.
-// TMEM columns: [0,128) S^T then P^T (fp16: queries 0-63 in [0,32), 64-127 in
-// [64,96)); [128,256) dP^T then
-// dQ; [256,384) dV; [384,512) dK.  dS is written to shared memory once, in the
+// TMEM columns: two 128-column regions, tile t in region t & 1, each holding
+// in turn S^T, P^T (fp16: queries 0-63 in its columns [0,32), 64-127 in
+// [64,96)), dP^T (after dV has read P^T) and dQ^T (after the math warps have
+// read dP^T); then [256,384) dV and [384,512) dK.  The next tile's scores go
+// into the other region as soon as the dQ^T left there has been read out, so
+// neither dP^T nor the scores wait for the dQ hand-off of the tile before.  dS is written to shared memory once, in the
 // 128-byte-swizzled layout that is K-major for dK = dS^T Q (A = dS^T) and
 // MN-major for dQ = dS K (A = dS).
 #include <cuda_bf16.h>
@@ -50,7 +53,9 @@ constexpr int kMath = 256;            // two math warpgroups
 constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile,
               kOffST = 6 * kTile;
 constexpr int kSmem = 7 * kTile + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+constexpr uint32_t kColDV = 256, kColDK = 384;
+// TMEM region (S^T, P^T, dP^T, dQ^T) of tile t
+__device__ __forceinline__ uint32_t region(int t) { return static_cast<uint32_t>(t & 1) * 128u; }
 
 struct Bars {
   uint64_t kv_full;
@@ -188,40 +193,46 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-          mma_ss(tmem + kColS, desc_kmajor_sw128(sK + off), desc_kmajor_sw128(qb + off), id_kk, k > 0);
+          mma_ss(tmem + region(t), desc_kmajor_sw128(sK + off), desc_kmajor_sw128(qb + off), id_kk, k > 0);
         }
         mma_commit(smem_u32(&bars.s_full));
         return true;
       };
       if (ok) ok = issue_qk(0);
       int nret = 0;
+      int pend = -1, pend_region = 0;       // retained tile whose dQ^T awaits read-out, and its region
       for (int t = 0; ok && t < ntiles; ++t) {
         if (!mbar_wait(smem_u32(&bars.p_ready), t & 1, abortp, a.status)) break;
         fence_after_sync();
         const int ret = flag;
         const uint32_t qb = sQ + (t & 1) * kTile;
+        const uint32_t rg = tmem + region(t);
         if (ret) {
           if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status)) break;
-          // dQ of the previous retained tile has left the dP columns
-          if (nret > 0 && !mbar_wait(smem_u32(&bars.dq_free), (nret - 1) & 1, abortp, a.status)) break;
           fence_after_sync();
-          // dP^T = V dO^T first: the math warps' dS work then overlaps dV and the next scores
+          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in the region's
+          // columns 0-31, queries 64-127 in columns 64-95, each written by its math group)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColDV, rg + (k / 4) * 64 + (k % 4) * 8,
+                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
+          // dP^T = V dO^T over P^T (read by dV above: MMAs execute in issue order)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-            mma_ss(tmem + kColDP, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
+            mma_ss(rg, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
           }
           mma_commit(smem_u32(&bars.dp_full));
-          // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in columns 0-31,
-          // queries 64-127 in columns 64-95, each written by its math group)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColDV, tmem + kColS + (k / 4) * 64 + (k % 4) * 8,
-                   desc_mnmajor_sw128(sDO + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars.do_empty));
         }
-        // the next scores overwrite P^T, which dV (issued above, executed in order) has read
-        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
+        // the next scores into the other region, once the dQ^T left there has been read out
+        if (t + 1 < ntiles) {
+          if (pend >= 0 && pend_region == ((t + 1) & 1)) {
+            if (!mbar_wait(smem_u32(&bars.dq_free), pend & 1, abortp, a.status)) break;
+            pend = -1;
+          }
+          if (!issue_qk(t + 1)) break;
+        }
         if (!ret) {
           mma_commit(smem_u32(&bars.q_empty[t & 1]));
           continue;
@@ -235,13 +246,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                  desc_mnmajor_sw128(qb + k * 2048, kHalf, 1024), id_kmn, (nret > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bars.q_empty[t & 1]));
         // dQ^T = K^T dS^T  (A = K tile read MN-major, B = the same dS tile read
-        // MN-major), into the dP columns: TMEM lane = head dim, column = query,
-        // so the read-out below adds whole 128-byte rows of dQ at once
+        // MN-major) over dP^T, which the math warps have read: TMEM lane = head
+        // dim, column = query, so the read-out adds whole 128-byte rows of dQ
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + kColDP, desc_mnmajor_sw128(sK + k * 2048, kHalf, 1024),
+          mma_ss(rg, desc_mnmajor_sw128(sK + k * 2048, kHalf, 1024),
                  desc_mnmajor_sw128(sDS + k * 2048, kHalf, 1024), id_mnmn, k > 0);
         mma_commit(smem_u32(&bars.dq_full));
+        pend = nret;
+        pend_region = t & 1;
         ++nret;
       }
       mma_commit(smem_u32(&bars.fin));
@@ -260,7 +273,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const float inv_sl2 = 1.f / sl2;
     int nret = 0, do_issued = 0, head_kept = 0;
     bool ok = true;
-    int prev_q0 = 0, prev_h = 0;   // query block / head of the last retained tile (for the dQ read-out)
+    // query block, head and TMEM region of the last retained tile (for its dQ
+    // read-out, one iteration later), and how many dQ tiles have been read out
+    int prev_q0 = 0, prev_h = 0;
+    uint32_t prev_rg = 0;
+    int flushed = 0;
 
     // per-query vectors of tile t (fetched by group 0 one tile ahead): lse and
     // D as loaded, and the decision threshold log2(tau / L_q).  The arithmetic
@@ -283,7 +300,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (ntiles > 0 && cg == 0) fetch(0);
 
     // Move the finished dQ^T tile (lane = head dim r, columns = queries) out of
-    // TMEM, release the dP columns, and add it into the fp32 accumulator with
+    // TMEM, release its region, and add it into the fp32 accumulator with
     // two bulk reduce-adds of 64 query rows: group 0 stages its rows in the dS
     // buffer (free: dK and dQ have consumed it), group 1 in the staging buffer.
     // Thread 0 owns the bulk groups.  Returns false on abort.
@@ -298,7 +315,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, v);
+          tmem_ld32_sync(lane_addr + prev_rg + 64 * cg + c * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * kD + r] = __uint_as_float(v[e]);
         }
@@ -344,7 +361,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t sr[32];
-          tmem_ld32_sync(lane_addr + kColS + 64 * cg + c * 32, sr);
+          tmem_ld32_sync(lane_addr + region(t) + 64 * cg + c * 32, sr);
           float gap = -INFINITY;
           if (interior) {
 #pragma unroll
@@ -380,6 +397,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           flag = 0;
           mbar_arrive(smem_u32(&bars.p_ready));
         }
+        // the previous retained tile's dQ is read out here too: the MMA warp
+        // waits for it before the scores of tile t + 1 go into its region
+        if (nret > flushed) {
+          if (!flush_dq(nret - 1, true)) break;
+          flushed = nret;
+        }
         continue;
       }
       if (tid == 0) {
@@ -400,7 +423,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t sr[32];
-        tmem_ld32_sync(lane_addr + kColS + 64 * cg + c * 32, sr);
+        tmem_ld32_sync(lane_addr + region(t) + 64 * cg + c * 32, sr);
         if (interior) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
@@ -422,7 +445,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           }
         }
       }
-      tmem_st32(lane_addr + kColS + 64 * cg, pk);   // inside this group's own S columns
+      tmem_st32(lane_addr + region(t) + 64 * cg, pk);   // inside this group's own S columns
       tmem_st_wait();
       fence_before_sync();
       if (named_vote_or(1, kMath, !ok || *abortp)) break;
@@ -430,8 +453,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         flag = 1;
         mbar_arrive(smem_u32(&bars.p_ready));
       }
-      // dQ of the previous retained tile leaves the dP columns before dP^T lands there
-      if (nret > 0 && !flush_dq(nret - 1, true)) break;
+      // the previous retained tile's dQ is read out while dV and dP^T run; the
+      // MMA warp waits for it only before the next scores go into its region
+      if (nret > flushed) {
+        if (!flush_dq(nret - 1, true)) break;
+        flushed = nret;
+      }
       ok = mbar_wait(smem_u32(&bars.dp_full), nret & 1, abortp, a.status);
       fence_after_sync();
       // dS^T = scale * P^T o (dP^T - D), fp16, computed into registers first so
@@ -443,7 +470,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dp[32];
-          tmem_ld32_sync(lane_addr + kColDP + 64 * cg + c * 32, dp);
+          tmem_ld32_sync(lane_addr + region(t) + 64 * cg + c * 32, dp);
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const float4 dd = d4[(c * 32 + 2 * e) / 4];
@@ -474,11 +501,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (tid == 0) mbar_arrive(smem_u32(&bars.ds_ready));
       prev_q0 = q0;
       prev_h = h;
+      prev_rg = region(t);
       ++nret;
     }
 
     // last dQ tile, then dK, dV out of TMEM (loads are warp-collective; stores per key)
-    if (nret > 0 && !*abortp) flush_dq(nret - 1, false);
+    if (nret > flushed && !*abortp) flush_dq(nret - 1, false);
     if (tid == 0) bulk_wait0();        // every reduce-add has landed before the CTA exits
     fence_after_sync();
     if (__all_sync(0xffffffffu, ok && !*abortp)) {
