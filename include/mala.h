@@ -165,6 +165,37 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
                         int32_t* retained_counts, uint8_t* tile_mask, void* stream);
 
 /*
+ * Variable-length MALA split-KV decode: mala_decode over a batch whose
+ * sequences hold different numbers of cached tokens (App. A.1; §2.1 counts
+ * L per query, and a decoding query's L is its own cache length, current
+ * token included).
+ *
+ * Sequence b attends to the first cache_lens[b] rows of its cache and tests
+ * tiles against log(tau / cache_lens[b]).  Its ceil(cache_lens[b] / block_k)
+ * tiles are cut into num_splits ranges exactly as mala_decode cuts a cache of
+ * that length, so each sequence gives what mala_decode gives on its cache
+ * truncated to cache_lens[b].
+ *
+ *  cache_lens [batch]                               int32, device memory, 4-byte aligned
+ *  k_cache, v_cache [batch, max_cache_len, heads_kv, head_dim]  (rows past a
+ *      sequence's length are never read into results)
+ *  tile_mask [batch, heads_kv, ceil(max_cache_len / block_k)]: entries of a
+ *      sequence's tiles past ceil(cache_lens[b] / block_k) are not written.
+ *  Everything else as mala_decode, with max_cache_len in place of cache_len.
+ *
+ * The lengths are read on the device.  A length outside [1, max_cache_len]
+ * sets bit 2 of the device status word (mala_device_status) and that
+ * sequence's o and lse come out NaN; the other sequences are unaffected.
+ * A null or misaligned cache_lens returns MALA_ERR_INVALID_ARG.
+ */
+mala_status mala_decode_varlen(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, const int32_t* cache_lens, int batch, int max_cache_len,
+                               int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                               mala_dtype out_dtype, int block_k, int num_splits, float tau,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/*
  * mala_decode without a workspace argument, for callers that cannot allocate
  * device memory: for example a serving process whose device memory is all
  * handed out by a fixed pool at start-up and that may not call cudaMalloc
@@ -200,9 +231,12 @@ size_t mala_decode_noalloc_max_floats(void);
 
 /*
  * Synchronise `stream`, then read and clear the device status word that the
- * kernels set when a bounded on-chip wait expires.  *device_code receives the
- * raw word (0 = no event).  Returns MALA_OK, MALA_ERR_TIMEOUT if the word was
- * set, or MALA_ERR_CUDA if synchronisation failed.
+ * kernels set.  Bits: 1 = a bounded on-chip wait expired (the kernel gave up
+ * and its outputs are not valid); 2 = mala_decode_varlen read a sequence
+ * length outside [1, max_cache_len].  *device_code receives the raw word
+ * (0 = no event).  Returns MALA_OK (word 0), MALA_ERR_TIMEOUT (bit 1 set),
+ * MALA_ERR_INVALID_ARG (any other bit), or MALA_ERR_CUDA if synchronisation
+ * failed.
  */
 mala_status mala_device_status(void* stream, int* device_code);
 

@@ -23,7 +23,7 @@ MALA_BF16, MALA_FP32 = 0, 1
 STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3: "MALA_ERR_WORKSPACE",
           4: "MALA_ERR_CUDA", 5: "MALA_ERR_TIMEOUT"}
 EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bwd",
-           "mala_decode_workspace_size", "mala_decode", "mala_decode_noalloc",
+           "mala_decode_workspace_size", "mala_decode", "mala_decode_varlen", "mala_decode_noalloc",
            "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
            "mala_last_cuda_error", "mala_cuda_error_string")
 
@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.mala_decode_workspace_size.argtypes = [_i] * 4
         L.mala_decode.restype = _i
         L.mala_decode.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
+        L.mala_decode_varlen.restype = _i
+        L.mala_decode_varlen.argtypes = [_vp] * 6 + [_i] * 9 + [_f, _f, _vp, _sz, _vp, _vp, _vp]
         L.mala_decode_noalloc.restype = _i
         L.mala_decode_noalloc.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _vp, _vp]
         L.mala_decode_noalloc_max_floats.restype = _sz
@@ -155,6 +157,21 @@ def mala_decode(q, k_cache, v_cache, o, lse, workspace, *, block=128, num_splits
         _stream(stream)))
 
 
+def mala_decode_varlen(q, k_cache, v_cache, o, lse, cache_lens, workspace, *, block=128, num_splits=16,
+                       tau=1.0, softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
+    """mala_decode with per-sequence cache lengths (int32 CUDA tensor [B]) over
+    caches padded to k_cache.shape[1]."""
+    B, Hq, D = q.shape
+    N, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if cache_lens.dtype != torch.int32 or cache_lens.shape != (B,):
+        raise ValueError("cache_lens must be an int32 tensor of shape [B]")
+    _check("mala_decode_varlen", lib().mala_decode_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), _ptr(cache_lens), B, N, Hq, Hkv, D,
+        _dt(q), _dt(o), block, num_splits, float(tau), _scale(D, softmax_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(retained_counts), _ptr(tile_mask),
+        _stream(stream)))
+
+
 def mala_decode_noalloc(q, k_cache, v_cache, o, lse, *, block=128, num_splits=16, tau=1.0,
                         softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
     """mala_decode with the split records in the library's fixed device array
@@ -170,7 +187,7 @@ def mala_decode_noalloc(q, k_cache, v_cache, o, lse, *, block=128, num_splits=16
 def mala_device_status(stream=None) -> int:
     code = _i(0)
     rc = lib().mala_device_status(_stream(stream), ctypes.byref(code))
-    if rc not in (0, 5):
+    if rc not in (0, 1, 5):     # OK, a rejected sequence length, an expired wait
         raise MalaError("mala_device_status", rc)
     return code.value
 
@@ -226,8 +243,9 @@ def backward(q, k, v, o, do, lse, tau=1.0, *, causal=True, block=128, softmax_sc
 
 
 def decode(q, k_cache, v_cache, tau=1.0, *, block=128, num_splits=16, softmax_scale=None,
-           out_dtype=None, counts=False, mask=False, stream=None):
-    """Returns (o, lse, info)."""
+           out_dtype=None, counts=False, mask=False, cache_lens=None, stream=None):
+    """Returns (o, lse, info).  `cache_lens` (int32 CUDA tensor [B]) selects
+    the variable-length decode over caches padded to k_cache.shape[1]."""
     B, Hq, D = q.shape
     N, Hkv = k_cache.shape[1], k_cache.shape[2]
     dev = q.device
@@ -239,7 +257,12 @@ def decode(q, k_cache, v_cache, tau=1.0, *, block=128, num_splits=16, softmax_sc
         info["counts"] = torch.zeros((B, Hkv, num_splits), dtype=torch.int32, device=dev)
     if mask:
         info["mask"] = torch.zeros((B, Hkv, _ntiles(N, block)), dtype=torch.uint8, device=dev)
-    mala_decode(q, k_cache, v_cache, o, lse, ws, block=block, num_splits=num_splits, tau=tau,
-                softmax_scale=softmax_scale, retained_counts=info.get("counts"),
-                tile_mask=info.get("mask"), stream=stream)
+    if cache_lens is None:
+        mala_decode(q, k_cache, v_cache, o, lse, ws, block=block, num_splits=num_splits, tau=tau,
+                    softmax_scale=softmax_scale, retained_counts=info.get("counts"),
+                    tile_mask=info.get("mask"), stream=stream)
+    else:
+        mala_decode_varlen(q, k_cache, v_cache, o, lse, cache_lens, ws, block=block, num_splits=num_splits,
+                           tau=tau, softmax_scale=softmax_scale, retained_counts=info.get("counts"),
+                           tile_mask=info.get("mask"), stream=stream)
     return o, lse, info

@@ -92,7 +92,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int hk = blockIdx.x, sp = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
-  const int T = (a.N + kBK - 1) / kBK;
+  const int n_b = decode_seq_len(a, b);                // this sequence's cache length
+  const int T = (n_b + kBK - 1) / kBK;
+  const int Tmax = (a.N + kBK - 1) / kBK;              // row length of the tile mask
   const int per = (T + a.splits - 1) / a.splits;
   const int t0 = sp * per, t1 = min(T, t0 + per);
   const int ntiles = max(0, t1 - t0);
@@ -194,7 +196,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
 
   // ---------------- score warps ----------------
   const bool test = a.tau > 0.f;
-  const float thr = a.log2_tau - log2f(static_cast<float>(a.N));
+  const float thr = a.log2_tau - log2f(static_cast<float>(n_b));
   const float sl2 = a.scale_log2;
   const int g = lane & 7;                        // the head this lane decides
 
@@ -246,7 +248,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
-        const bool valid = kbase_idx + 16 * mt + gq + 8 * hrow < a.N;
+        const bool valid = kbase_idx + 16 * mt + gq + 8 * hrow < n_b;
         acc[mt][2 * hrow] = valid ? acc[mt][2 * hrow] * sl2 : -INFINITY;
         acc[mt][2 * hrow + 1] = valid ? acc[mt][2 * hrow + 1] * sl2 : -INFINITY;
         mx0 = fmaxf(mx0, acc[mt][2 * hrow]);
@@ -270,7 +272,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     const float lt = (xl[t & 1][0][g] + xl[t & 1][1][g]) + (xl[t & 1][2][g] + xl[t & 1][3][g]);
     const bool keep_g = g < G && (lt == 0.f || !(tm - m_g - lg2(lt) < thr));
     const bool keep = !test || __any_sync(0xffffffffu, keep_g);
-    if (a.mask != nullptr && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * T + j] = keep ? 1 : 0;
+    if (a.mask != nullptr && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
     if (!keep) continue;
     ++kept;
     const int vs = nret % kNV;

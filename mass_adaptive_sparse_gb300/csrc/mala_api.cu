@@ -103,6 +103,54 @@ BwdLayout bwd_layout(int batch, int seqlen_q, int seqlen_k, int heads_q, int hea
   return w;
 }
 
+// Argument checks shared by the decode entry points (workspace excepted).
+mala_status check_decode(const void* q, const void* k_cache, const void* v_cache, const void* o,
+                         const float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                         int head_dim, int in_dtype, int out_dtype, int block_k, int num_splits,
+                         float tau, float softmax_scale) {
+  const void* ptrs[] = {q, k_cache, v_cache, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
+  if (batch < 1 || cache_len < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv != 0)
+    return MALA_ERR_INVALID_ARG;
+  if (batch > 65535 || heads_kv > 65535) return MALA_ERR_INVALID_ARG;
+  if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return MALA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MALA_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > 256 || block_k < 1 || head_dim < 1) return MALA_ERR_INVALID_ARG;
+  const int g = heads_q / heads_kv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
+  if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
+  return MALA_OK;
+}
+
+// Split kernel (tensor-core or CUDA-core) then the exact merge.
+mala_status run_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                       const int32_t* cache_lens, int batch, int cache_len, int heads_q, int heads_kv,
+                       int head_dim, int in_dtype, int out_dtype, int block_k, int num_splits, float tau,
+                       float softmax_scale, float* partial, int32_t* retained_counts, uint8_t* tile_mask,
+                       int* status, void* stream) {
+  DecArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
+  a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.lens = cache_lens;
+  a.in_dt = in_dtype; a.out_dt = out_dtype; a.blk = block_k; a.splits = num_splits;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.partial = partial;
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = decode_mma_supported(a) ? launch_decode_mma(a, s, &launches) : launch_decode_simt(a, s, &launches);
+  if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
+  return finish(e, launches);
+}
+
+bool workspace_ok(const void* workspace, size_t workspace_bytes, size_t need) {
+  return workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 && workspace_bytes >= need;
+}
+
 }  // namespace
 
 extern "C" {
@@ -206,38 +254,35 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
                         int num_splits, float tau, float softmax_scale,
                         void* workspace, size_t workspace_bytes,
                         int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
-  const void* ptrs[] = {q, k_cache, v_cache, o, lse};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
-  if (batch < 1 || cache_len < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv != 0)
-    return MALA_ERR_INVALID_ARG;
-  if (batch > 65535 || heads_kv > 65535) return MALA_ERR_INVALID_ARG;
-  if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return MALA_ERR_INVALID_ARG;
-  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MALA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 256 || block_k < 1 || head_dim < 1) return MALA_ERR_INVALID_ARG;
-  const int g = heads_q / heads_kv;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
-  if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
-  const size_t need = mala_decode_workspace_size(batch, heads_q, head_dim, num_splits);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+  const mala_status c = check_decode(q, k_cache, v_cache, o, lse, batch, cache_len, heads_q, heads_kv, head_dim,
+                                     in_dtype, out_dtype, block_k, num_splits, tau, softmax_scale);
+  if (c != MALA_OK) return c;
+  if (!workspace_ok(workspace, workspace_bytes, mala_decode_workspace_size(batch, heads_q, head_dim, num_splits)))
     return MALA_ERR_WORKSPACE;
   int* status = status_word();
   if (!status) return MALA_ERR_CUDA;
-  DecArgs a{};
-  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
-  a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
-  a.in_dt = in_dtype; a.out_dt = out_dtype; a.blk = block_k; a.splits = num_splits;
-  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.partial = static_cast<float*>(workspace);
-  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int launches = 0;
-  cudaError_t e = decode_mma_supported(a) ? launch_decode_mma(a, s, &launches) : launch_decode_simt(a, s, &launches);
-  if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
-  return finish(e, launches);
+  return run_decode(q, k_cache, v_cache, o, lse, nullptr, batch, cache_len, heads_q, heads_kv, head_dim, in_dtype,
+                    out_dtype, block_k, num_splits, tau, softmax_scale, static_cast<float*>(workspace),
+                    retained_counts, tile_mask, status, stream);
+}
+
+mala_status mala_decode_varlen(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, const int32_t* cache_lens, int batch, int max_cache_len,
+                               int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                               mala_dtype out_dtype, int block_k, int num_splits, float tau,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  if (!cache_lens || (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return MALA_ERR_INVALID_ARG;
+  const mala_status c = check_decode(q, k_cache, v_cache, o, lse, batch, max_cache_len, heads_q, heads_kv,
+                                     head_dim, in_dtype, out_dtype, block_k, num_splits, tau, softmax_scale);
+  if (c != MALA_OK) return c;
+  if (!workspace_ok(workspace, workspace_bytes, mala_decode_workspace_size(batch, heads_q, head_dim, num_splits)))
+    return MALA_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  return run_decode(q, k_cache, v_cache, o, lse, cache_lens, batch, max_cache_len, heads_q, heads_kv, head_dim,
+                    in_dtype, out_dtype, block_k, num_splits, tau, softmax_scale, static_cast<float*>(workspace),
+                    retained_counts, tile_mask, status, stream);
 }
 
 mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
@@ -245,38 +290,17 @@ mala_status mala_decode_noalloc(const void* q, const void* k_cache, const void* 
                                 int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
                                 int num_splits, float tau, float softmax_scale,
                                 int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
-  const void* ptrs[] = {q, k_cache, v_cache, o, lse};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
-  if (batch < 1 || cache_len < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv != 0)
-    return MALA_ERR_INVALID_ARG;
-  if (batch > 65535 || heads_kv > 65535) return MALA_ERR_INVALID_ARG;
-  if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return MALA_ERR_INVALID_ARG;
-  if (!(tau >= 0.f) || !std::isfinite(tau)) return MALA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return MALA_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > 256 || block_k < 1 || head_dim < 1) return MALA_ERR_INVALID_ARG;
-  const int g = heads_q / heads_kv;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return MALA_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
-  if (block_k != 64 && block_k != 128) return MALA_ERR_UNSUPPORTED;
+  const mala_status c = check_decode(q, k_cache, v_cache, o, lse, batch, cache_len, heads_q, heads_kv, head_dim,
+                                     in_dtype, out_dtype, block_k, num_splits, tau, softmax_scale);
+  if (c != MALA_OK) return c;
   const size_t need = static_cast<size_t>(num_splits) * batch * heads_q * (head_dim + 4);
   if (need > kNoAllocDecodeFloats) return MALA_ERR_WORKSPACE;
   float* scratch = decode_scratch();
   int* status = status_word();
   if (!scratch || !status) return MALA_ERR_CUDA;
-  DecArgs a{};
-  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
-  a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
-  a.in_dt = in_dtype; a.out_dt = out_dtype; a.blk = block_k; a.splits = num_splits;
-  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.partial = scratch;
-  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int launches = 0;
-  cudaError_t e = decode_mma_supported(a) ? launch_decode_mma(a, s, &launches) : launch_decode_simt(a, s, &launches);
-  if (e == cudaSuccess) e = launch_decode_merge(a, s, &launches);
-  return finish(e, launches);
+  return run_decode(q, k_cache, v_cache, o, lse, nullptr, batch, cache_len, heads_q, heads_kv, head_dim, in_dtype,
+                    out_dtype, block_k, num_splits, tau, softmax_scale, scratch, retained_counts, tile_mask,
+                    status, stream);
 }
 
 size_t mala_decode_noalloc_max_floats(void) { return kNoAllocDecodeFloats; }
@@ -289,7 +313,8 @@ mala_status mala_device_status(void* stream, int* device_code) {
   const int zero = 0;
   if (word != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MALA_ERR_CUDA;
   *device_code = word;
-  return word == 0 ? MALA_OK : MALA_ERR_TIMEOUT;
+  if (word & kStatusWaitTimeout) return MALA_ERR_TIMEOUT;
+  return word == 0 ? MALA_OK : MALA_ERR_INVALID_ARG;
 }
 
 uint64_t mala_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

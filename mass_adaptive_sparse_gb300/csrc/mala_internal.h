@@ -16,8 +16,8 @@ enum Dtype : int { kBF16 = 0, kFP32 = 1 };
 
 // Device status word codes (bitwise OR of events).
 enum StatusCode : int {
-  kStatusWaitTimeout = 1,   // an mbarrier / flag wait hit its iteration cap
-  kStatusBadLaunch = 2      // a kernel found its launch shape inconsistent
+  kStatusWaitTimeout = 1,   // an mbarrier wait ran past its time limit
+  kStatusBadLength = 2      // a variable-length decode sequence length was outside [1, N]
 };
 
 struct FwdArgs {
@@ -48,7 +48,8 @@ struct BwdArgs {
 
 struct DecArgs {
   const void* q; const void* k; const void* v; void* o; float* lse;
-  int B, N, Hq, Hkv, D;
+  int B, N, Hq, Hkv, D;     // N: cache length (the padded length when `lens` is set)
+  const int32_t* lens;      // per-sequence cache lengths [B] (device), or null: all N
   int in_dt, out_dt, blk, splits;
   float tau, log2_tau, scale_log2;
   float* partial;       // workspace: [splits, B, Hq, D + 4] = (m, l, l_rounded, 0, u[D]), m in log2 units;
@@ -57,6 +58,21 @@ struct DecArgs {
   uint8_t* mask;        // [B, Hkv, T] or null
   int* status;
 };
+
+#ifdef __CUDACC__
+// Cache length of sequence b: N, or lens[b] for a variable-length decode.  A
+// length outside [1, N] raises kStatusBadLength and gives 0 (no keys: the
+// sequence's output and lse come out NaN).
+__device__ __forceinline__ int decode_seq_len(const DecArgs& a, int b) {
+  if (a.lens == nullptr) return a.N;
+  const int n = a.lens[b];
+  if (n < 1 || n > a.N) {
+    atomicOr(a.status, kStatusBadLength);
+    return 0;
+  }
+  return n;
+}
+#endif
 
 // Each launcher returns the first CUDA error and adds its launches to *launches.
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s, int* launches);

@@ -333,11 +333,13 @@ decode_split_simt_kernel(const DecArgs a) {
   const Tin* qg = static_cast<const Tin*>(a.q);
   const Tin* kg = static_cast<const Tin*>(a.k);
   const Tin* vg = static_cast<const Tin*>(a.v);
-  const int T = (a.N + BK - 1) / BK;
+  const int n_b = decode_seq_len(a, b);                // this sequence's cache length
+  const int T = (n_b + BK - 1) / BK;
+  const int Tmax = (a.N + BK - 1) / BK;                // row length of the tile mask
   const int per = (T + a.splits - 1) / a.splits;
   const int t0 = sp * per, t1 = min(T, t0 + per);
   const bool test = a.tau > 0.f;
-  const float thr = a.log2_tau - log2f(static_cast<float>(a.N));
+  const float thr = a.log2_tau - log2f(static_cast<float>(n_b));
 
   for (int idx = tid; idx < G * D; idx += NT) {
     const int g = idx / D, c = idx % D;
@@ -353,14 +355,14 @@ decode_split_simt_kernel(const DecArgs a) {
     __syncthreads();
     for (int idx = tid; idx < BK * D; idx += NT) {
       const int kr = idx / D, c = idx % D, key = k0 + kr;
-      Ks[kr][c] = key < a.N ? ld(kg + ((static_cast<size_t>(b) * a.N + key) * a.Hkv + hk) * D + c) : 0.f;
+      Ks[kr][c] = key < n_b ? ld(kg + ((static_cast<size_t>(b) * a.N + key) * a.Hkv + hk) * D + c) : 0.f;
     }
     __syncthreads();
     float mloc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
     for (int kr = tid; kr < BK; kr += NT) {
-      const bool valid = k0 + kr < a.N;
+      const bool valid = k0 + kr < n_b;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float s = 0.f;
@@ -389,12 +391,12 @@ decode_split_simt_kernel(const DecArgs a) {
       if (test && (l[g] == 0.f || !(x - m[g] - log2f(l[g]) < thr))) keep = true;
     }
     if (a.mask != nullptr && tid == 0)
-      a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * T + j] = keep ? 1 : 0;
+      a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
     if (!keep) continue;
     ++kept;
     for (int idx = tid; idx < BK * D; idx += NT) {
       const int kr = idx / D, c = idx % D, key = k0 + kr;
-      Vs[kr][c] = key < a.N ? ld(vg + ((static_cast<size_t>(b) * a.N + key) * a.Hkv + hk) * D + c) : 0.f;
+      Vs[kr][c] = key < n_b ? ld(vg + ((static_cast<size_t>(b) * a.N + key) * a.Hkv + hk) * D + c) : 0.f;
     }
     float mnew[G], alpha[G], psum[G];
 #pragma unroll
@@ -475,9 +477,10 @@ __global__ void decode_merge_kernel(const DecArgs a) {
       const float ls = base[s * stride + 1];
       if (ls > 0.f) u += exp2f(base[s * stride] - mmax) * base[s * stride + 4 + c];
     }
-    st(static_cast<Tout*>(a.o) + (static_cast<size_t>(b) * a.Hq + h) * D + c, u / lrsum);
+    // a sequence with no keys (a rejected length) has lsum = 0: NaN output
+    st(static_cast<Tout*>(a.o) + (static_cast<size_t>(b) * a.Hq + h) * D + c, lsum > 0.f ? u / lrsum : NAN);
   }
-  if (threadIdx.x == 0) a.lse[static_cast<size_t>(b) * a.Hq + h] = (mmax + log2f(lsum)) * kLn2;
+  if (threadIdx.x == 0) a.lse[static_cast<size_t>(b) * a.Hq + h] = lsum > 0.f ? (mmax + log2f(lsum)) * kLn2 : NAN;
 }
 
 // ---------------------------------------------------------------------------

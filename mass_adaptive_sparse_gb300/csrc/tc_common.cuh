@@ -77,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
-        atomicOr(status, 1);
+        atomicOr(status, 1);        // kStatusWaitTimeout
         return false;
       }
     }

@@ -44,7 +44,7 @@ __all__ = [
     "visible_key_counts", "dense_attention", "dense_attention_grads",
     "restricted_attention", "mala_forward", "mala_backward",
     "block_summary", "merge_summaries", "mala_decode",
-    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd",
+    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd", "mala_decode_varlen_bhd",
     "omitted_mass", "BORDERLINE_REL",
 ]
 
@@ -463,4 +463,34 @@ def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=Non
             lse[b, hk * grp:(hk + 1) * grp] = r.lse
             retained[b, hk] = r.retained
             margin[b, hk] = r.margin
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+
+
+def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_splits, batches=None):
+    """Variable-length decode: sequence b attends to the first cache_lens[b]
+    rows of its (padded) cache, which hold its current token, so its L is
+    cache_lens[b] (§2.1: L counts the query's own causal context; App. A.1
+    for the split-KV decode).  Each sequence is exactly ``mala_decode`` on its
+    truncated cache.  retained / margin are [B, Hkv, ceil(N_max / bk)], with
+    tiles past a sequence's own tiles left False / NaN."""
+    bsz, hq, d = q.shape
+    n_max, hkv = k_cache.shape[1], k_cache.shape[2]
+    grp = hq // hkv
+    t_max = -(-n_max // bk)
+    o = np.zeros((bsz, hq, v_cache.shape[3]))
+    lse = np.full((bsz, hq), np.nan)
+    retained = np.zeros((bsz, hkv, t_max), dtype=bool)
+    margin = np.full((bsz, hkv, t_max), np.nan)
+    for b in (range(bsz) if batches is None else batches):
+        n = int(cache_lens[b])
+        if not 1 <= n <= n_max:
+            raise ValueError(f"cache length {n} of sequence {b} is outside [1, {n_max}]")
+        t = -(-n // bk)
+        for hk in range(hkv):
+            r = mala_decode(q[b, hk * grp:(hk + 1) * grp], k_cache[b, :n, hk], v_cache[b, :n, hk],
+                            scale, tau, bk, num_splits)
+            o[b, hk * grp:(hk + 1) * grp] = r.o
+            lse[b, hk * grp:(hk + 1) * grp] = r.lse
+            retained[b, hk, :t] = r.retained
+            margin[b, hk, :t] = r.margin
     return {"o": o, "lse": lse, "retained": retained, "margin": margin}

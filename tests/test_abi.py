@@ -106,3 +106,14 @@ def test_noalloc_decode_rejects_oversize_before_any_launch(lib):
 
 def test_device_status_rejects_null(lib):
     assert lib.mala_device_status(None, None) == 1
+
+
+def test_decode_varlen_rejects_missing_or_misaligned_lengths(lib):
+    args = [FAKE] * 5
+    shape = [8, 1024, 32, 8, 128, 0, 0, 128, 16, 1.0, 0.08, FAKE, 1 << 30, None, None, None]
+    assert lib.mala_decode_varlen(*args, None, *shape) == 1
+    assert lib.mala_decode_varlen(*args, ctypes.c_void_p(0x10002), *shape) == 1
+    # shape checks are those of mala_decode
+    bad = list(shape)
+    bad[2], bad[3] = 48, 3                      # group of 16
+    assert lib.mala_decode_varlen(*args, FAKE, *bad) == 2

@@ -13,7 +13,10 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None):
+def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None, lens=None):
+    """Decode on the GPU and compare with the oracle; `lens` (one cache length
+    per sequence, each in [1, N]) selects the variable-length entry point over
+    caches padded to N."""
     x = synthetic.decode_inputs(cfg, N=N, B=B, seed=seed)
     q, k, v = x["q"], x["k"], x["v"]
     if d is not None:
@@ -22,25 +25,33 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
         q, k, v = q.to(dtype), k.to(dtype), v.to(dtype)
     D = q.shape[-1]
     scale = 1 / math.sqrt(D)
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
     o, lse, info = api.decode(q.cuda(), k.cuda(), v.cuda(), tau, block=block, num_splits=splits,
-                              counts=True, mask=True)
+                              counts=True, mask=True, cache_lens=lens_t)
     torch.cuda.synchronize()
     assert api.mala_device_status() == 0
     batches = list(range(B)) if batches is None else batches
     q64, k64, v64 = (parity.to64(t) for t in (q, k, v))
-    ref = orc.mala_decode_bhd(q64, k64, v64, scale, tau, block, splits, batches=batches)
+    if lens is None:
+        ref = orc.mala_decode_bhd(q64, k64, v64, scale, tau, block, splits, batches=batches)
+    else:
+        ref = orc.mala_decode_varlen_bhd(q64, k64, v64, lens, scale, tau, block, splits, batches=batches)
     go, glse, gmask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
     Hq, Hkv = q.shape[1], k.shape[2]
     grp = Hq // Hkv
-    T = -(-N // block)
-    per = -(-T // splits)
     fp32 = q.dtype == torch.float32
     ok = np.zeros((B, Hq), bool)
     flipped = 0
+    counts = info["counts"].cpu().numpy()
     for b in batches:
+        n_b = N if lens is None else lens[b]
+        T = -(-n_b // block)
+        per = -(-T // splits)
         for hk in range(Hkv):
-            diff = gmask[b, hk].astype(bool) != ref["retained"][b, hk]
+            diff = gmask[b, hk, :T].astype(bool) != ref["retained"][b, hk, :T]
             hs = slice(hk * grp, (hk + 1) * grp)
+            for sp in range(splits):
+                np.testing.assert_array_equal(counts[b, hk, sp], gmask[b, hk, sp * per:min(T, (sp + 1) * per)].sum())
             if not diff.any():
                 ok[b, hs] = True
                 continue
@@ -50,16 +61,13 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
                 if idx:
                     assert parity.is_borderline(ref["margin"][b, hk, idx[0]])
             flipped += 1
-            keep = gmask[b, hk].astype(bool)[None, :]
-            o_r, lse_r = orc.restricted_attention(q64[b, hs], k64[b, :, hk], v64[b, :, hk], scale, keep,
+            keep = gmask[b, hk, :T].astype(bool)[None, :]
+            o_r, lse_r = orc.restricted_attention(q64[b, hs], k64[b, :n_b, hk], v64[b, :n_b, hk], scale, keep,
                                                   grp, block, causal=False)
             parity.check_close("o (flipped)", go[b, hs], o_r, q.dtype, fp32=fp32)
     assert flipped <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * Hkv)
     m = parity.check_close("o", go[ok], ref["o"][ok], q.dtype, fp32=fp32)
     assert np.abs(glse[ok] - ref["lse"][ok]).max() <= parity.LSE_ABS
-    counts = info["counts"].cpu().numpy()
-    for sp in range(splits):
-        np.testing.assert_array_equal(counts[:, :, sp], gmask[:, :, sp * per:min(T, (sp + 1) * per)].sum(-1))
     return m, gmask
 
 
@@ -101,3 +109,41 @@ def test_decode_128k_full_size_sampled():
     cfg = synthetic.CONFIGS["decode_128k"]
     for tau in (1.0, 0.0):
         _check(cfg, cfg.N, cfg.B, tau, cfg.num_splits, cfg.block, cfg.seed, batches=[0, 5])
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.0])
+def test_decode_varlen_bf16(tau):
+    """Per-sequence cache lengths over a cache padded to 1500 rows: one row,
+    a partial tile, exactly one tile, one row past a tile, and the full cache."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 1500, 6, tau, 4, 128, 61, lens=[1, 77, 128, 129, 1000, 1500])
+
+
+def test_decode_varlen_fp32_d64():
+    """The CUDA-core split kernel (fp32, head_dim 64, 64-key tiles)."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 700, 4, 1.0, 5, 64, 67, dtype=torch.float32, d=64, lens=[700, 1, 333, 64])
+
+
+def test_decode_varlen_rejects_bad_lengths_per_sequence():
+    """A length of 0 or past the padded cache raises status bit 2 and gives NaN
+    for that sequence only; the others match the oracle."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    N, B = 600, 4
+    lens = [300, 0, 601, 600]
+    x = synthetic.decode_inputs(cfg, N=N, B=B, seed=71)
+    q, k, v = x["q"], x["k"], x["v"]
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o, lse, _ = api.decode(q.cuda(), k.cuda(), v.cuda(), 1.0, block=128, num_splits=4, cache_lens=lens_t)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 2
+    assert api.mala_device_status() == 0          # reading clears the word
+    go, glse = parity.to64(o), parity.to64(lse)
+    assert np.isnan(go[1]).all() and np.isnan(go[2]).all()
+    assert np.isnan(glse[1]).all() and np.isnan(glse[2]).all()
+    q64, k64, v64 = (parity.to64(t) for t in (q, k, v))
+    ref = orc.mala_decode_varlen_bhd(q64, k64, v64, [300, 1, 1, 600], 1 / math.sqrt(128), 1.0, 128, 4,
+                                     batches=[0, 3])
+    for b in (0, 3):
+        parity.check_close("o", go[b], ref["o"][b], q.dtype)
+        assert np.abs(glse[b] - ref["lse"][b]).max() <= parity.LSE_ABS

@@ -404,3 +404,39 @@ def test_decode_split_output_is_renormalised_softmax_and_bounded():
         _, lse_d = orc.dense_attention(qg, kc, vc, scale, causal=False)
         assert np.all(orc.omitted_mass(r.lse, lse_d) <= 0.5)
         assert keep.shape == (4, 32)
+
+
+def test_decode_varlen_uses_each_sequence_length_uniform_scores():
+    """Uniform scores (q = 0) make every decision a closed form.  A 100-token
+    sequence in a cache padded to 200 rows, 32-key tiles, one split, tau = 4:
+    the newest (4-key) tile is retained (l = 0), the next gives ratio
+    -log 4 >= log(4/100) and is retained (l = 36), the older two give
+    -log 36 < log(4/100) and are skipped.  With L = 200 instead, tile 1 would
+    be retained (-log 36 >= log(4/200)).  The output is the mean of v over
+    keys 64..99 (the retained keys).  The full 200-row cache (L = 200, newest
+    tile of 8 keys) keeps tiles 6, 5, 4 (-log 40 >= log(4/200) > -log 72)."""
+    n_max, n = 200, 100
+    q = np.zeros((1, 2, 8))
+    k = _rand((1, n_max, 1, 8), 91)
+    v = _rand((1, n_max, 1, 8), 92)
+    r = orc.mala_decode_varlen_bhd(q, k, v, [n], 0.5, 4.0, 32, 1)
+    assert r["retained"][0, 0].tolist() == [False, False, True, True, False, False, False]
+    np.testing.assert_allclose(r["o"][0, 0], v[0, 64:100, 0].mean(axis=0), rtol=1e-13)
+    np.testing.assert_allclose(r["lse"][0], math.log(36.0), rtol=1e-13)
+    full = orc.mala_decode_varlen_bhd(q, k, v, [n_max], 0.5, 4.0, 32, 1)
+    assert full["retained"][0, 0].tolist() == [False, False, False, False, True, True, True]
+    np.testing.assert_allclose(full["o"][0, 0], v[0, 128:200, 0].mean(axis=0), rtol=1e-13)
+    np.testing.assert_allclose(full["lse"][0], math.log(72.0), rtol=1e-13)
+
+
+@pytest.mark.parametrize("lens,splits", [([40, 200, 1, 129], 3), ([200, 200, 200, 200], 4)])
+def test_decode_varlen_tau0_is_dense_over_each_prefix(lens, splits):
+    """tau = 0: each sequence's output is plain softmax attention over its own
+    first cache_lens[b] keys."""
+    q = _rand((4, 2, 16), 93, 2.0)
+    k, v = _rand((4, 200, 1, 16), 94), _rand((4, 200, 1, 16), 95)
+    r = orc.mala_decode_varlen_bhd(q, k, v, lens, 0.25, 0.0, 32, splits)
+    for b, n in enumerate(lens):
+        o_ref, lse_ref = _sdpa(q[b], k[b, :n, 0], v[b, :n, 0], 0.25, causal=False)
+        np.testing.assert_allclose(r["o"][b], o_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r["lse"][b], lse_ref, rtol=1e-12, atol=1e-12)
