@@ -76,6 +76,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+
+__device__ __forceinline__ uint32_t pack_f16_2(uint64_t v) {
+  float lo, hi;
+  f2_split(v, lo, hi);
+  return pack_f16(lo, hi);
+}
+
 template <typename Tg>
 __device__ __forceinline__ void store_grad_row(Tg* dst, const uint32_t* v, float scale);
 
@@ -341,8 +348,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         // lse in log2 units; scale * D (dS = P (scale dP - scale D)); the
         // threshold on the raw dot product (keep iff raw S >= c)
         const float l2 = n_lse * kLog2e;
-        vec_lse[r] = l2;
-        vec_d[r] = n_d * a.scale;
+        vec_lse[r] = -l2;                     // negated: P = exp2(S * scale_log2 + vec_lse)
+        vec_d[r] = -n_d * a.scale;            // negated: dS = P (scale dP + vec_d)
         vec_c[r] = n_thr == INFINITY ? INFINITY : (l2 + n_thr) * inv_sl2;
       }
       named_sync(1, kMath);
@@ -419,6 +426,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       // P^T = exp2(S * scale_log2 - lse) in fp16, written over this group's S columns
       const float4* l4 = reinterpret_cast<const float4*>(&vec_lse[64 * cg]);
+      const uint64_t sl2x2 = f2(sl2, sl2);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -428,10 +436,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float4 ll = l4[(c * 32 + e) / 4];
-            pk[c * 16 + e / 2] = pack_f16(ex2(fmaf(__uint_as_float(sr[e]), sl2, -ll.x)),
-                                          ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -ll.y)));
-            pk[c * 16 + e / 2 + 1] = pack_f16(ex2(fmaf(__uint_as_float(sr[e + 2]), sl2, -ll.z)),
-                                              ex2(fmaf(__uint_as_float(sr[e + 3]), sl2, -ll.w)));
+            float x0, x1, x2, x3;
+            f2_split(fma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2(ll.x, ll.y)), x0, x1);
+            f2_split(fma2(f2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2, f2(ll.z, ll.w)), x2, x3);
+            pk[c * 16 + e / 2] = pack_f16(ex2(x0), ex2(x1));
+            pk[c * 16 + e / 2 + 1] = pack_f16(ex2(x2), ex2(x3));
           }
         } else {
 #pragma unroll
@@ -439,8 +448,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const int q = 64 * cg + c * 32 + e;
             const bool l0 = key_ok && q < qlim && q >= qmin;
             const bool l1 = key_ok && q + 1 < qlim && q + 1 >= qmin;
-            const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[e]), sl2, -vec_lse[q])) : 0.f;
-            const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -vec_lse[q + 1])) : 0.f;
+            const float p0 = l0 ? ex2(fmaf(__uint_as_float(sr[e]), sl2, vec_lse[q])) : 0.f;
+            const float p1 = l1 ? ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, vec_lse[q + 1])) : 0.f;
             pk[c * 16 + e / 2] = pack_f16(p0, p1);
           }
         }
@@ -466,7 +475,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       uint32_t w[32];
       if (__all_sync(0xffffffffu, ok)) {
         const float4* d4 = reinterpret_cast<const float4*>(&vec_d[64 * cg]);
-        const float sc = a.scale;
+        const uint64_t sc2 = f2(a.scale, a.scale);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t dp[32];
@@ -475,10 +484,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           for (int e = 0; e < 16; e += 2) {
             const float4 dd = d4[(c * 32 + 2 * e) / 4];
             const uint32_t pw0 = pk[c * 16 + e], pw1 = pk[c * 16 + e + 1];
-            w[c * 16 + e] = pack_f16(f16_lo(pw0) * fmaf(sc, __uint_as_float(dp[2 * e]), -dd.x),
-                                     f16_hi(pw0) * fmaf(sc, __uint_as_float(dp[2 * e + 1]), -dd.y));
-            w[c * 16 + e + 1] = pack_f16(f16_lo(pw1) * fmaf(sc, __uint_as_float(dp[2 * e + 2]), -dd.z),
-                                         f16_hi(pw1) * fmaf(sc, __uint_as_float(dp[2 * e + 3]), -dd.w));
+            const uint64_t t0 = fma2(f2(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), sc2,
+                                     f2(dd.x, dd.y));
+            const uint64_t t1 = fma2(f2(__uint_as_float(dp[2 * e + 2]), __uint_as_float(dp[2 * e + 3])), sc2,
+                                     f2(dd.z, dd.w));
+            w[c * 16 + e] = pack_f16_2(mul2(f2(f16_lo(pw0), f16_hi(pw0)), t0));
+            w[c * 16 + e + 1] = pack_f16_2(mul2(f2(f16_lo(pw1), f16_hi(pw1)), t1));
           }
         }
       }

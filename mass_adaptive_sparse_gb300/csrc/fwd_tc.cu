@@ -54,6 +54,7 @@ struct Bars {
   uint64_t fin;
 };
 
+
 template <typename Tout>
 __device__ __forceinline__ void store_row(Tout* dst, const float* v, float scale);
 
@@ -272,15 +273,25 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
       const float nscale = a.scale_log2;
-      float rowsum = 0.f, rowsum_r = 0.f;
+      const uint64_t nsc2 = f2(nscale, nscale), nm2 = f2(-mref, -mref);
+      uint64_t acc = f2(0.f, 0.f), accr = f2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), nscale, -mref));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), nscale, -mref));
+        float e0, e1;
+        f2_split(fma2(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), nsc2, nm2), e0, e1);
+        const float p0 = ex2(e0), p1 = ex2(e1);
         const uint32_t w = pack_bf16(p0, p1);
-        rowsum += p0 + p1;
-        rowsum_r += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        acc = add2(acc, f2(p0, p1));
+        accr = add2(accr, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
         sr[c] = w;                            // P packed over the consumed scores
+      }
+      float rowsum, rowsum_r;
+      {
+        float x0, x1;
+        f2_split(acc, x0, x1);
+        rowsum = x0 + x1;
+        f2_split(accr, x0, x1);
+        rowsum_r = x0 + x1;
       }
       xsum[cg][r] = rowsum;
       xsumr[cg][r] = rowsum_r;
