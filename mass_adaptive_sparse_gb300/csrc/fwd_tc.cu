@@ -237,13 +237,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
       }
       xmax[cg][r] = mraw;
-      named_sync(1, kSoft);
+      fence_before_sync();
+      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also the barrier for xmax
       const float mt = fmaxf(xmax[0][r], xmax[1][r]) * a.scale_log2;
       const bool has = valid && lim >= j * kBlk;
       const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
-      fence_before_sync();
       const int keep = named_vote_or(1, kSoft, keep_row);
-      if (named_vote_or(1, kSoft, !ok || *abortp)) break;
       if (!keep) {
         if (tid == 0) {
           flag[sb] = 0;
