@@ -388,8 +388,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
       }
       fence_before_sync();
-      const int keep = named_vote_or(1, kMath, keep_row);
-      if (named_vote_or(1, kMath, !ok || *abortp)) break;
+      // an abort is caught at the vote after P^T is stored, or (skipped tiles)
+      // by the next tile's waits, which return at once once the flag is up
+      const int keep = named_vote_or(1, kMath, keep_row && ok);
       uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + i) * Tc + kb : nullptr;
       if (tid == 0) {
         head_kept += keep;
