@@ -111,7 +111,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     mbar_init(smem_u32(&bars.q_full), 1);
     for (int i = 0; i < kNK; ++i) { mbar_init(smem_u32(&bars.k_full[i]), 1); mbar_init(smem_u32(&bars.k_empty[i]), 1); }
     for (int i = 0; i < kNV; ++i) { mbar_init(smem_u32(&bars.v_full[i]), 1); mbar_init(smem_u32(&bars.v_empty[i]), 1); }
-    for (int i = 0; i < kNS; ++i) { mbar_init(smem_u32(&bars.s_full[i]), 1); mbar_init(smem_u32(&bars.sm_done[i]), 1); }
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.sm_done[i]), kSoft / 32);     // one arrival per softmax warp
+    }
     mbar_init(smem_u32(&bars.pv_done[0]), 1);
     mbar_init(smem_u32(&bars.pv_done[1]), 1);
     mbar_init(smem_u32(&bars.fin), 1);
@@ -209,6 +212,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // row state, identical in both groups: l is the exact fp32 sum of P (Eq. 3
     // test and lse); lr sums the bf16-rounded P that enters the P V product
     float m_used = -INFINITY, l = 0.f, lr = 0.f;
+    // the other group's row sums of a retained tile are read a tile later,
+    // after the next row-max barrier has published them
+    float alpha_pend = 1.f;
+    bool sum_pend = false;
     int nret = 0, vissued = 0;
     bool ok = true;
     uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc : nullptr;
@@ -238,7 +245,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       xmax[cg][r] = mraw;
       fence_before_sync();
-      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also the barrier for xmax
+      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also the barrier for xmax, xsum
+      if (sum_pend) {
+        l = l * alpha_pend + (xsum[0][r] + xsum[1][r]);
+        lr = lr * alpha_pend + (xsumr[0][r] + xsumr[1][r]);
+        sum_pend = false;
+      }
       const float mt = fmaxf(xmax[0][r], xmax[1][r]) * a.scale_log2;
       const bool has = valid && lim >= j * kBlk;
       const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
@@ -246,9 +258,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (!keep) {
         if (tid == 0) {
           flag[sb] = 0;
-          mbar_arrive(smem_u32(&bars.sm_done[sb]));
           if (mask_row) mask_row[j] = 0;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.sm_done[sb]));
         continue;
       }
       if (tid == 0) {
@@ -313,14 +326,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       tmem_st32(lane_addr + sb * 128 + 64 * cg, sr);   // inside this group's own S columns
       tmem_st_wait();
       fence_before_sync();
-      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also publishes xsum / xsumr
-      l = l * alpha + (xsum[0][r] + xsum[1][r]);
-      lr = lr * alpha + (xsumr[0][r] + xsumr[1][r]);
-      if (tid == 0) {
-        flag[sb] = 1;
-        mbar_arrive(smem_u32(&bars.sm_done[sb]));
-      }
+      // each warp hands its P over once its TMEM stores are complete (an abort
+      // is caught by the next tile's first vote)
+      if (tid == 0) flag[sb] = 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.sm_done[sb]));
+      alpha_pend = alpha;
+      sum_pend = true;
       ++nret;
+    }
+    named_sync(1, kSoft);                     // publishes the last tile's row sums
+    if (sum_pend) {
+      l = l * alpha_pend + (xsum[0][r] + xsum[1][r]);
+      lr = lr * alpha_pend + (xsumr[0][r] + xsumr[1][r]);
     }
 
     // epilogue: wait for the last P V, then O / l and lse = m + log l
