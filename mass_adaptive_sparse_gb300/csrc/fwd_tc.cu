@@ -254,7 +254,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const float mt = fmaxf(xmax[0][r], xmax[1][r]) * a.scale_log2;
       const bool has = valid && lim >= j * kBlk;
       const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
-      const int keep = named_vote_or(1, kSoft, keep_row);
+      // both groups hold every row's full maximum, so each votes alone (same result)
+      const int keep = named_vote_or(2 + cg, 128, keep_row);
       if (!keep) {
         if (tid == 0) {
           flag[sb] = 0;
