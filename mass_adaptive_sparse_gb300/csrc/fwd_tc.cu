@@ -7,21 +7,35 @@
 // rowmax(S) - m - log l < log(tau / L_q) (l = 0 keeps).  A skipped tile issues
 // no V load and no P V product and leaves (m, l, O) unchanged (App. A.1).
 //
-// One CTA = one query block of one head, 320 threads:
-//   warps 0-7  softmax, two warpgroups: thread (c, r) owns columns [64c, 64c+64)
-//              of query row r = TMEM lane r.  The groups combine the row max
-//              and row sums through shared memory (each keeps a copy of the
-//              row state), vote on the tile, and for retained tiles thread 0
-//              issues the V load; P = exp2(S - m) goes as bf16 into TMEM
-//              inside each group's own S columns.
-//   warp 8     TMA producer for Q and K (2-stage K ring).
-//   warp 9     MMA issuer: S = Q K^T (SS, K-major operands) and
-//              O += P V (A = P from TMEM, B = V MN-major), accumulate in TMEM.
-// TMEM: three S buffers (columns 0, 128, 256) and O (columns 384..511), so
-// scores run two tiles ahead of the softmax while a retained tile waits for
-// its V.  The running max is only moved when it grows by more than 2^8
-// (log2 units); P and l are kept relative to the max in use, which leaves
-// m + log l = log Z unchanged, so the test is unaffected.
+// One CTA = two adjacent query blocks (slots 0 and 1) of one head; both walk
+// the same key blocks, so each K tile is loaded once for the pair.  384 threads;
+// warps 0-3 hold the control roles:
+//   warps 0, 3  sequencers, one thread per slot: O_s += P_s V, then at once the
+//              slot's next S_s = Q_s K^T.  The tensor pipe takes new MMAs only
+//              as it drains, so each sequencer gathers everything its turn
+//              needs (vote, P, V, K) first, then takes the turn from the other
+//              by a token barrier.  The slots thus alternate on the pipe in a
+//              fixed order, one slot's softmax overlapping the other slot's
+//              MMAs, and only the hand-off separates two MMA groups.  A K or V
+//              stage is released by one commit per slot.  Warp 3 also owns TMEM.
+//   warp 1     V loader (one thread): follows the votes in step order and loads
+//              the V tile of a key block once a slot keeps it.  The 2-stage V
+//              ring takes one phase per step; a step that no slot keeps
+//              completes its phase with a plain arrival.  A sequencer ends
+//              each step only once the loader has seen all of its votes, and
+//              votes and keep flags alternate between two barriers / words by
+//              step parity, so no wait can meet a phase from two steps later.
+//   warp 2     TMA producer: both Q tiles once, then a 3-stage K ring.
+//   warps 4-7  softmax of slot 0, warps 8-11 softmax of slot 1: thread r owns
+//              query row r of its slot (TMEM lane r) and all 128 columns, so
+//              the row max, the Eq. 3 test and the row sums need no exchange;
+//              the slot's 128 rows vote on the tile with one barrier reduction.
+// TMEM: S_0 (columns 0-127), S_1 (128-255), O_0 (256-383), O_1 (384-511).
+// P (bf16) is written over the first 64 columns of the slot's S; the next
+// Q K^T of that slot is issued after its P V on the same tensor pipe, which
+// executes them in order.  The running max is only moved when it grows by more
+// than 2^8 (log2 units); P and l are kept relative to the max in use, which
+// leaves m + log l = log Z unchanged, so the test is unaffected.
 #include <cuda_bf16.h>
 
 #include "mala_internal.h"
@@ -36,24 +50,25 @@ constexpr int kD = 128;                 // head dim
 constexpr int kBlk = 128;               // B_q = B_k
 constexpr int kTile = kBlk * kD * 2;    // 32 KiB: one 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;        // one 64-column TMA box
-constexpr int kNK = 2;                  // K stages
-constexpr int kNV = 3;                  // V stages
-constexpr int kNS = 3;                  // S buffers in TMEM
-constexpr int kThreads = 320;
-constexpr int kSoft = 256;              // two softmax warpgroups
-constexpr int kSmem = kTile * (1 + kNK + kNV) + 1024;
-constexpr uint32_t kColO = 384;
+constexpr int kNK = 3;                  // K stages
+constexpr int kNV = 2;                  // V stages
+constexpr int kThreads = 384;
+constexpr int kSmem = kTile * (2 + kNK + kNV) + 1024;
+constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.0f;        // move the running max only past 2^8 growth
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kNK], k_empty[kNK];
   uint64_t v_full[kNV], v_empty[kNV];
-  uint64_t s_full[kNS], sm_done[kNS];
-  uint64_t pv_done[2];
-  uint64_t fin;
+  uint64_t s_full[2];     // Q K^T of the slot complete (so is its previous P V)
+  uint64_t dec[2][2];     // [slot][step parity]: the slot's rows voted (keep_flag written), S read out
+  uint64_t p_ready[2];    // P of a kept tile is in TMEM (one arrival per warp)
+  uint64_t o_done[2];     // every MMA of the slot complete
+  uint64_t vl_done[2];    // [step parity]: the V loader has seen every vote of the step
+  uint64_t tok[2];        // [slot]: the other slot's sequencer has taken its turn
+  uint64_t fin[2];        // every MMA of a sequencer complete (its own wait before exit)
 };
-
 
 template <typename Tout>
 __device__ __forceinline__ void store_row(Tout* dst, const float* v, float scale);
@@ -80,6 +95,28 @@ __device__ __forceinline__ void store_row<float>(float* dst, const float* v, flo
     d4[i] = make_float4(v[4 * i] * scale, v[4 * i + 1] * scale, v[4 * i + 2] * scale, v[4 * i + 3] * scale);
 }
 
+// Scores of the columns past `last` (the last legal one) become -inf.
+__device__ __forceinline__ void mask_cols(uint32_t* sr, int last) {
+#pragma unroll
+  for (int c = 0; c < 64; ++c)
+    if (c > last) sr[c] = 0xff800000u;
+}
+
+// 64 raw scores -> 32 packed bf16 pairs of P = exp2(S * scale - m) in sr[0..31];
+// acc sums P exactly, accr sums P as rounded to bf16 (two lanes per register).
+__device__ __forceinline__ void exp_pack(uint32_t* sr, uint64_t nsc2, uint64_t nm2, uint64_t& acc, uint64_t& accr) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float e0, e1;
+    f2_split(fma2(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), nsc2, nm2), e0, e1);
+    const float p0 = ex2(e0), p1 = ex2(e1);
+    const uint32_t w = pack_bf16(p0, p1);
+    acc = add2(acc, f2(p0, p1));
+    accr = add2(accr, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+    sr[c] = w;
+  }
+}
+
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -87,37 +124,56 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_sh;
-  __shared__ int flag[kNS];
+  __shared__ int keep_flag[2][2];     // [slot][step parity]
   __shared__ int abort_flag;
-  __shared__ float xmax[2][kBlk], xsum[2][kBlk], xsumr[2][kBlk];   // per-group row partials
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = base;
-  const uint32_t sK = base + kTile;
-  const uint32_t sV = base + kTile * (1 + kNK);
+  const uint32_t sQ = base;                       // slot s at sQ + s * kTile
+  const uint32_t sK = base + 2 * kTile;
+  const uint32_t sV = base + kTile * (2 + kNK);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int bh = blockIdx.x;
   const int h = bh % a.Hq, b = bh / a.Hq;
   const int Tr = (a.Lq + kBlk - 1) / kBlk, Tc = (a.Lk + kBlk - 1) / kBlk;
-  const int qb = Tr - 1 - static_cast<int>(blockIdx.y);          // heaviest query blocks first
+  const int pair = (Tr + 1) / 2 - 1 - static_cast<int>(blockIdx.y);   // heaviest pairs first
+  const int nslots = (2 * pair + 1 < Tr) ? 2 : 1;
   const int hk = h / (a.Hq / a.Hkv);
-  const int jtop = a.causal ? min(Tc - 1, (min(a.Lq, qb * kBlk + kBlk) - 1) / kBlk) : Tc - 1;
+  // top key block of each slot; the pair walks from the higher one down to 0
+  int jtop_s[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int qb = 2 * pair + s;
+    jtop_s[s] = a.causal ? min(Tc - 1, (min(a.Lq, qb * kBlk + kBlk) - 1) / kBlk) : Tc - 1;
+  }
+  if (nslots == 1) jtop_s[1] = -1;
+  const int jtop = max(jtop_s[0], jtop_s[1]);
   const int ntiles = jtop + 1;
+  // slot s takes part in steps t >= first[s] (key block jtop - t); its local
+  // step is u = t - first[s].  The two slots' first steps differ by at most one.
+  const int first0 = jtop - jtop_s[0];
+  const int first1 = nslots == 2 ? jtop - jtop_s[1] : ntiles;
 
-  if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_sh));
+  if (warp == 3) tmem_alloc<512>(smem_u32(&tmem_sh));
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bars.q_full), 1);
-    for (int i = 0; i < kNK; ++i) { mbar_init(smem_u32(&bars.k_full[i]), 1); mbar_init(smem_u32(&bars.k_empty[i]), 1); }
-    for (int i = 0; i < kNV; ++i) { mbar_init(smem_u32(&bars.v_full[i]), 1); mbar_init(smem_u32(&bars.v_empty[i]), 1); }
-    for (int i = 0; i < kNS; ++i) {
-      mbar_init(smem_u32(&bars.s_full[i]), 1);
-      mbar_init(smem_u32(&bars.sm_done[i]), kSoft / 32);     // one arrival per softmax warp
+    // a K or V stage is released by one arrival per slot
+    for (int i = 0; i < kNK; ++i) { mbar_init(smem_u32(&bars.k_full[i]), 1); mbar_init(smem_u32(&bars.k_empty[i]), nslots); }
+    for (int i = 0; i < kNV; ++i) { mbar_init(smem_u32(&bars.v_full[i]), 1); mbar_init(smem_u32(&bars.v_empty[i]), nslots); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.s_full[s]), 1);
+      mbar_init(smem_u32(&bars.dec[s][0]), 1);
+      mbar_init(smem_u32(&bars.dec[s][1]), 1);
+      mbar_init(smem_u32(&bars.p_ready[s]), 4);   // one arrival per warp of the slot
+      mbar_init(smem_u32(&bars.o_done[s]), 1);
     }
-    mbar_init(smem_u32(&bars.pv_done[0]), 1);
-    mbar_init(smem_u32(&bars.pv_done[1]), 1);
-    mbar_init(smem_u32(&bars.fin), 1);
+    mbar_init(smem_u32(&bars.vl_done[0]), 1);
+    mbar_init(smem_u32(&bars.vl_done[1]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars.tok[i]), 1);
+      mbar_init(smem_u32(&bars.fin[i]), 1);
+    }
     fence_barrier_init();
   }
   fence_before_sync();
@@ -126,250 +182,295 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const uint32_t tmem = tmem_sh;
   volatile int* abortp = &abort_flag;
 
-  if (warp == 8) {
-    // ---------------- TMA producer: Q once, then the K ring ----------------
+  if (warp == 2) {
+    // ---------------- TMA producer: Q tiles once, then the K ring ----------------
     if (lane == 0) {
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
-      prefetch_tensormap(&mv);
       const uint32_t qf = smem_u32(&bars.q_full);
-      mbar_expect_tx(qf, kTile);
-      tma_load_4d(sQ, &mq, qf, 0, h, qb * kBlk, b);
-      tma_load_4d(sQ + kHalf, &mq, qf, 64, h, qb * kBlk, b);
+      mbar_expect_tx(qf, kTile * nslots);
+      for (int s = 0; s < nslots; ++s) {
+        const int row = (2 * pair + s) * kBlk;
+        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, b);
+        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, b);
+      }
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kNK, n = t / kNK;
-        if (n > 0 && !mbar_wait(smem_u32(&bars.k_empty[s]), (n - 1) & 1, abortp, a.status)) break;
-        const uint32_t kf = smem_u32(&bars.k_full[s]);
+        const int st = t % kNK, n = t / kNK;
+        if (n > 0 && !mbar_wait(smem_u32(&bars.k_empty[st]), (n - 1) & 1, abortp, a.status)) break;
+        const uint32_t kf = smem_u32(&bars.k_full[st]);
         const int row = (jtop - t) * kBlk;
         mbar_expect_tx(kf, kTile);
-        tma_load_4d(sK + s * kTile, &mk, kf, 0, hk, row, b);
-        tma_load_4d(sK + s * kTile + kHalf, &mk, kf, 64, hk, row, b);
+        tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, b);
+        tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, b);
         ++issued;
       }
-      // drain: every issued load has landed before the CTA can finish
+      // every issued load lands before the CTA can finish
+      mbar_drain(smem_u32(&bars.q_full), 0, a.status);
       for (int t = max(0, issued - kNK); t < issued; ++t)
-        mbar_wait(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, abortp, a.status);
+        mbar_drain(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, a.status);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1) {
+    // ---------------- V loader ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(1, 0, 0, kBlk, kBlk);
-      constexpr uint32_t idesc_pv = idesc_f16(1, 0, 1, kBlk, kD);
-      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abortp, a.status);
-      auto issue_qk = [&](int t) -> bool {
-        const int s = t % kNK, n = t / kNK;
-        if (!mbar_wait(smem_u32(&bars.k_full[s]), n & 1, abortp, a.status)) return false;
-        fence_after_sync();
-        const uint32_t d = tmem + (t % kNS) * 128;
-        const uint32_t kbase = sK + s * kTile;
+      prefetch_tensormap(&mv);
+      const int first[2] = {first0, first1};
+      int armed = -1;              // last step whose V phase this thread armed
+      for (int t = 0; t < ntiles; ++t) {
+        const int vs = t % kNV;
+        bool load = false, ok = true;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-          mma_ss(d, desc_kmajor_sw128(sQ + off), desc_kmajor_sw128(kbase + off), idesc_qk, k > 0);
-        }
-        mma_commit(smem_u32(&bars.k_empty[s]));
-        mma_commit(smem_u32(&bars.s_full[t % kNS]));
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      if (ok && ntiles > 1) ok = issue_qk(1);
-      int npv = 0;
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int sb = t % kNS;
-        if (!mbar_wait(smem_u32(&bars.sm_done[sb]), (t / kNS) & 1, abortp, a.status)) break;
-        fence_after_sync();
-        if (t + 2 < ntiles && !issue_qk(t + 2)) break;
-        if (flag[sb]) {
-          const int vs = npv % kNV;
-          if (!mbar_wait(smem_u32(&bars.v_full[vs]), (npv / kNV) & 1, abortp, a.status)) break;
-          fence_after_sync();
-          const uint32_t vbase = sV + vs * kTile;
-          // P: keys 0-63 packed in columns 0-31 of the S buffer, keys 64-127 in 64-95
-          const uint32_t p_tmem = tmem + sb * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColO, p_tmem + (k / 4) * 64 + (k % 4) * 8, desc_mnmajor_sw128(vbase + k * 2048, kHalf, 1024),
-                   idesc_pv, (npv > 0 || k > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bars.v_empty[vs]));
-          mma_commit(smem_u32(&bars.pv_done[npv & 1]));
-          ++npv;
-        }
-      }
-      // all MMAs of this thread complete before TMEM is released
-      mma_commit(smem_u32(&bars.fin));
-      mbar_wait(smem_u32(&bars.fin), 0, abortp, a.status);
-    }
-  } else {
-    // ---------------- softmax: thread (cg, r) = columns [64cg, 64cg+64) of row r ----------------
-    const int r = tid & 127, cg = tid >> 7;
-    const int qrow = qb * kBlk + r;
-    const bool valid = qrow < a.Lq;
-    const int lim = a.causal ? min(qrow, a.Lk - 1) : a.Lk - 1;   // last legal key of this row
-    const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk));
-    const bool test = a.tau > 0.f;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    // row state, identical in both groups: l is the exact fp32 sum of P (Eq. 3
-    // test and lse); lr sums the bf16-rounded P that enters the P V product
-    float m_used = -INFINITY, l = 0.f, lr = 0.f;
-    // the other group's row sums of a retained tile are read a tile later,
-    // after the next row-max barrier has published them
-    float alpha_pend = 1.f;
-    bool sum_pend = false;
-    int nret = 0, vissued = 0;
-    bool ok = true;
-    uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc : nullptr;
-
-    for (int t = 0; t < ntiles; ++t) {
-      const int j = jtop - t, sb = t % kNS;
-      ok = mbar_wait(smem_u32(&bars.s_full[sb]), (t / kNS) & 1, abortp, a.status);
-      fence_after_sync();
-      uint32_t sr[64];                        // raw scores Q.K of this group's columns, later packed P
-      if (__all_sync(0xffffffffu, ok)) tmem_ld64_sync(lane_addr + sb * 128 + 64 * cg, sr);
-      // row max over legal keys (raw dot products; the scale is positive).
-      // Interior tiles (not diagonal, no ragged edge) need no masking.
-      const int cmax = valid ? lim - j * kBlk - 64 * cg : -1;
-      const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= a.Lk) && (qb + 1) * kBlk <= a.Lq;
-      float mraw = -INFINITY;
-      if (interior) {
-#pragma unroll
-        for (int c = 0; c < 64; c += 2)
-          mraw = fmaxf(mraw, fmaxf(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = (c <= cmax) ? __uint_as_float(sr[c]) : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          mraw = fmaxf(mraw, x);
-        }
-      }
-      xmax[cg][r] = mraw;
-      fence_before_sync();
-      if (named_vote_or(1, kSoft, !ok || *abortp)) break;   // also the barrier for xmax, xsum
-      if (sum_pend) {
-        l = l * alpha_pend + (xsum[0][r] + xsum[1][r]);
-        lr = lr * alpha_pend + (xsumr[0][r] + xsumr[1][r]);
-        sum_pend = false;
-      }
-      const float mt = fmaxf(xmax[0][r], xmax[1][r]) * a.scale_log2;
-      const bool has = valid && lim >= j * kBlk;
-      const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
-      // both groups hold every row's full maximum, so each votes alone (same result)
-      const int keep = named_vote_or(2 + cg, 128, keep_row);
-      if (!keep) {
-        if (tid == 0) {
-          flag[sb] = 0;
-          if (mask_row) mask_row[j] = 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars.sm_done[sb]));
-        continue;
-      }
-      if (tid == 0) {
-        // V of this tile: loaded only now that the tile is retained
-        const int vs = vissued % kNV, n = vissued / kNV;
-        if (n > 0) ok = mbar_wait(smem_u32(&bars.v_empty[vs]), (n - 1) & 1, abortp, a.status);
-        if (ok) {
-          const uint32_t vf = smem_u32(&bars.v_full[vs]);
-          mbar_expect_tx(vf, kTile);
-          tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBlk, b);
-          tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBlk, b);
-          ++vissued;
-        }
-        if (mask_row) mask_row[j] = 1;
-      }
-      // online update (Algorithm 1), with a lazily moved reference max
-      float alpha = 1.f;
-      if (has && mt > m_used + kRescale) {
-        alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - mt);
-        m_used = mt;
-      }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      const float nscale = a.scale_log2;
-      const uint64_t nsc2 = f2(nscale, nscale), nm2 = f2(-mref, -mref);
-      uint64_t acc = f2(0.f, 0.f), accr = f2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float e0, e1;
-        f2_split(fma2(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), nsc2, nm2), e0, e1);
-        const float p0 = ex2(e0), p1 = ex2(e1);
-        const uint32_t w = pack_bf16(p0, p1);
-        acc = add2(acc, f2(p0, p1));
-        accr = add2(accr, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
-        sr[c] = w;                            // P packed over the consumed scores
-      }
-      float rowsum, rowsum_r;
-      {
-        float x0, x1;
-        f2_split(acc, x0, x1);
-        rowsum = x0 + x1;
-        f2_split(accr, x0, x1);
-        rowsum_r = x0 + x1;
-      }
-      xsum[cg][r] = rowsum;
-      xsumr[cg][r] = rowsum_r;
-      // O must be rescaled when the reference max moved: wait for the last P V
-      if (nret > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const int prev = nret - 1;
-        if (ok) ok = mbar_wait(smem_u32(&bars.pv_done[prev & 1]), (prev >> 1) & 1, abortp, a.status);
-        fence_after_sync();
-        if (__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32_sync(lane_addr + kColO + 64 * cg + c * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_addr + kColO + 64 * cg + c * 32, o);
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || t < first[s]) continue;
+          const int u = t - first[s];
+          ok = mbar_wait(smem_u32(&bars.dec[s][u & 1]), (u >> 1) & 1, abortp, a.status);
+          if (ok && !load && keep_flag[s][u & 1]) {
+            // the stage's previous step (t - 2) is done with it
+            if (t >= kNV) ok = mbar_wait(smem_u32(&bars.v_empty[vs]), (t / kNV - 1) & 1, abortp, a.status);
+            if (ok) {
+              const uint32_t vf = smem_u32(&bars.v_full[vs]);
+              mbar_expect_tx(vf, kTile);
+              tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, (jtop - t) * kBlk, b);
+              tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, (jtop - t) * kBlk, b);
+              load = true;
+              armed = t;
+            }
           }
         }
+        if (!ok) break;
+        if (!load) {
+          // no slot keeps this key block: complete the step's phase without a load
+          if (t >= kNV && !mbar_wait(smem_u32(&bars.v_empty[vs]), (t / kNV - 1) & 1, abortp, a.status)) break;
+          mbar_arrive(smem_u32(&bars.v_full[vs]));
+          armed = t;
+        }
+        mbar_arrive(smem_u32(&bars.vl_done[t & 1]));
       }
-      tmem_st32(lane_addr + sb * 128 + 64 * cg, sr);   // inside this group's own S columns
-      tmem_st_wait();
-      fence_before_sync();
-      // each warp hands its P over once its TMEM stores are complete (an abort
-      // is caught by the next tile's first vote)
-      if (tid == 0) flag[sb] = 1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars.sm_done[sb]));
-      alpha_pend = alpha;
-      sum_pend = true;
-      ++nret;
+      // loads of the last armed steps land before the CTA can finish
+      for (int t = max(0, armed - 1); t <= armed; ++t)
+        mbar_drain(smem_u32(&bars.v_full[t % kNV]), (t / kNV) & 1, a.status);
     }
-    named_sync(1, kSoft);                     // publishes the last tile's row sums
-    if (sum_pend) {
-      l = l * alpha_pend + (xsum[0][r] + xsum[1][r]);
-      lr = lr * alpha_pend + (xsumr[0][r] + xsumr[1][r]);
-    }
-
-    // epilogue: wait for the last P V, then O / l and lse = m + log l
-    if (ok && !*abortp && nret > 0) {
-      const int last = nret - 1;
-      ok = mbar_wait(smem_u32(&bars.pv_done[last & 1]), (last >> 1) & 1, abortp, a.status);
-    }
-    fence_after_sync();
-    if (__all_sync(0xffffffffu, ok && !*abortp)) {
-      Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
-      const float inv = 1.f / lr;
+  } else if (warp == 0 || warp == 3) {
+    // ---------------- sequencers: one thread per slot, turns passed by token ----------------
+    const int s = warp == 0 ? 0 : 1;
+    if (lane == 0 && s < nslots) {
+      constexpr uint32_t idesc_qk = idesc_f16(1, 0, 0, kBlk, kBlk);
+      constexpr uint32_t idesc_pv = idesc_f16(1, 0, 1, kBlk, kD);
+      const int first = s == 0 ? first0 : first1;
+      const bool solo = nslots == 1;
+      // the slot whose first step comes first takes the first turn
+      const bool leads = solo || (s == 0 ? first0 <= first1 : first1 < first0);
+      const uint64_t dq = desc_kmajor_sw128(sQ + s * kTile);
+      const uint32_t d_s = tmem + s * 128, d_o = tmem + kColO + s * 128;
+      int turn = 0;                // turns taken
+      // wait for the other slot's last turn (its MMAs are then queued ahead)
+      auto take_turn = [&]() -> bool {
+        const int k = leads ? turn - 1 : turn;
+        return solo || k < 0 || mbar_wait(smem_u32(&bars.tok[s]), k & 1, abortp, a.status);
+      };
+      auto pass_turn = [&]() {
+        if (!solo) mbar_arrive(smem_u32(&bars.tok[1 - s]));
+        ++turn;
+      };
+      int kwaited = first - 1;     // K stages waited for, in step order
+      auto wait_k = [&](int t) -> bool {
+        while (kwaited < t) {
+          ++kwaited;
+          if (!mbar_wait(smem_u32(&bars.k_full[kwaited % kNK]), (kwaited / kNK) & 1, abortp, a.status))
+            return false;
+        }
+        return true;
+      };
+      // S_s = Q_s K(t)^T, reported at once
+      auto issue_qk = [&](int t) {
+        const uint64_t dk = desc_kmajor_sw128(sK + (t % kNK) * kTile);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float o[32];
-        tmem_ld32_sync(lane_addr + kColO + 64 * cg + c * 32, reinterpret_cast<uint32_t*>(o));
-        if (valid) store_row<Tout>(orow + 64 * cg + c * 32, o, inv);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = ((k / 4) * kHalf + (k % 4) * 32) >> 4;
+          mma_ss(d_s, dq + off, dk + off, idesc_qk, k > 0);
+        }
+        mma_commit(smem_u32(&bars.s_full[s]));
+      };
+      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abortp, a.status);
+      // steps before this slot's first one: it reads neither their K nor their V
+      for (int t = 0; t < first; ++t) {
+        mbar_arrive(smem_u32(&bars.k_empty[t % kNK]));
+        mbar_arrive(smem_u32(&bars.v_empty[t % kNV]));
       }
-      if (valid && cg == 0) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m_used + log2f(l)) * kLn2;
-      if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = nret;
+      // turn 0: the slot's first product
+      ok = ok && wait_k(first) && take_turn();
+      if (ok) {
+        fence_after_sync();
+        issue_qk(first);
+        pass_turn();
+        mma_commit(smem_u32(&bars.k_empty[first % kNK]));
+      }
+      int nkeep = 0;
+      for (int t = first; ok && t < ntiles; ++t) {
+        const int vs = t % kNV, u = t - first;
+        const bool more = t + 1 < ntiles;
+        // everything this turn needs, gathered before taking it
+        ok = mbar_wait(smem_u32(&bars.dec[s][u & 1]), (u >> 1) & 1, abortp, a.status);
+        const bool keep = ok && keep_flag[s][u & 1];
+        if (keep)
+          ok = mbar_wait(smem_u32(&bars.p_ready[s]), nkeep & 1, abortp, a.status) &&
+               mbar_wait(smem_u32(&bars.v_full[vs]), (t / kNV) & 1, abortp, a.status);
+        if (ok && more) ok = wait_k(t + 1);
+        ok = ok && take_turn();
+        if (!ok) break;
+        fence_after_sync();
+        if (keep) {
+          // O_s += P_s V: P of keys 0-63 in columns 0-31 of S_s, keys 64-127 in 64-95
+          const uint64_t dv = desc_mnmajor_sw128(sV + vs * kTile, kHalf, 1024);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(d_o, d_s + (k / 4) * 64 + (k % 4) * 8, dv + ((k * 2048) >> 4), idesc_pv,
+                   (nkeep > 0 || k > 0) ? 1u : 0u);
+          ++nkeep;
+        }
+        if (more) {
+          issue_qk(t + 1);
+        } else {
+          mma_commit(smem_u32(&bars.o_done[s]));
+        }
+        pass_turn();
+        if (more) mma_commit(smem_u32(&bars.k_empty[(t + 1) % kNK]));
+        // The V loader has seen every vote of this step (and waited for the
+        // stage's previous phase) before this slot releases the stage or
+        // takes its next turn, so no barrier completes a phase ahead of its waiter.
+        ok = mbar_wait(smem_u32(&bars.vl_done[t & 1]), (t >> 1) & 1, abortp, a.status);
+        if (ok) mma_commit(smem_u32(&bars.v_empty[vs]));
+      }
+      // all MMAs of this thread complete before TMEM is released
+      mma_commit(smem_u32(&bars.fin[s]));
+      mbar_drain(smem_u32(&bars.fin[s]), 0, a.status);
     }
-    // V loads issued but never consumed (abort path) must land before exit
-    if (tid == 0) {
-      for (int n = max(0, vissued - kNV); n < vissued; ++n)
-        mbar_wait(smem_u32(&bars.v_full[n % kNV]), (n / kNV) & 1, abortp, a.status);
+  } else if (warp >= 4) {
+    // ---------------- softmax: thread r of slot s owns query row r ----------------
+    const int s = (warp >> 2) - 1, r = tid & 127;
+    if (s < nslots) {
+      const int qb = 2 * pair + s;
+      const int qrow = qb * kBlk + r;
+      const bool valid = qrow < a.Lq;
+      const int lim = a.causal ? min(qrow, a.Lk - 1) : a.Lk - 1;   // last legal key of this row
+      const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk));
+      const bool test = a.tau > 0.f;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      const uint32_t colS = s * 128, colO = kColO + s * 128;
+      // row state: l is the exact fp32 sum of P (Eq. 3 test and lse); lr sums
+      // the bf16-rounded P that enters the P V product (normalises O)
+      float m_used = -INFINITY, l = 0.f, lr = 0.f;
+      int nret = 0, it = 0;
+      bool ok = true;
+      uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc : nullptr;
+      const int t0 = jtop - jtop_s[s];
+
+      // After a timed-out wait the loop runs on without breaking (waits then
+      // fail at once), so the slot's barrier reductions always stay matched.
+      for (int t = t0; t < ntiles; ++t) {
+        const int j = jtop - t;
+        ok = mbar_wait(smem_u32(&bars.s_full[s]), it & 1, abortp, a.status) && ok;
+        ++it;
+        fence_after_sync();
+        // S is streamed in two 64-column halves (64 live scores per thread):
+        // the max pass reads both, the exponent pass reuses the second half
+        // still in registers and reloads the first.
+        // Interior tiles (not diagonal, no ragged edge) need no masking.
+        const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= a.Lk) && (qb + 1) * kBlk <= a.Lq;
+        const int cmax = valid ? lim - j * kBlk : -1;   // last legal column of this row in the tile
+        uint32_t sr[64];                        // raw scores Q.K of one half, later packed P
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_ld64_sync(lane_addr + colS + 64 * hf, sr);
+          if (!interior) mask_cols(sr, cmax - 64 * hf);
+          // row max over legal keys (raw dot products; the scale is positive)
+#pragma unroll
+          for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
+        }
+        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = mraw * a.scale_log2;
+        const bool has = valid && lim >= j * kBlk;
+        const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
+        fence_before_sync();                    // the S read-out precedes the hand-back
+        const int keep = named_vote_or(1 + s, 128, keep_row);
+        const int u = it - 1;                   // local step of this slot
+        if (r == 0) {
+          keep_flag[s][u & 1] = keep;
+          if (mask_row) mask_row[j] = static_cast<uint8_t>(keep);
+          mbar_arrive(smem_u32(&bars.dec[s][u & 1]));
+        }
+        if (!keep) continue;
+        ++nret;
+        // online update (Algorithm 1), with a lazily moved reference max
+        float alpha = 1.f;
+        if (has && mt > m_used + kRescale) {
+          alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - mt);
+          m_used = mt;
+        }
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        const uint64_t nsc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
+        uint64_t acc = f2(0.f, 0.f), accr = f2(0.f, 0.f);
+        // P = exp2(S * scale - m_ref) as bf16 pairs; P of keys 64-127 goes over
+        // the (consumed) scores of keys 64-95, P of keys 0-63 over keys 0-31
+        exp_pack(sr, nsc2, nm2, acc, accr);
+        tmem_st32(lane_addr + colS + 64, sr);
+        tmem_ld64_sync(lane_addr + colS, sr);
+        if (!interior) mask_cols(sr, cmax);
+        exp_pack(sr, nsc2, nm2, acc, accr);
+        float rowsum, rowsum_r;
+        {
+          float x0, x1;
+          f2_split(acc, x0, x1);
+          rowsum = x0 + x1;
+          f2_split(accr, x0, x1);
+          rowsum_r = x0 + x1;
+        }
+        // O rescale when the reference max moved.  The slot's previous P V is
+        // complete: it was issued before the Q K^T whose completion s_full reported.
+        if (nret > 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32_sync(lane_addr + colO + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_addr + colO + c * 32, o);
+          }
+        }
+        tmem_st32(lane_addr + colS, sr);
+        tmem_st_wait();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars.p_ready[s]));   // P is in TMEM
+        l = l * alpha + rowsum;
+        lr = lr * alpha + rowsum_r;
+      }
+
+      // epilogue: every MMA of the slot complete, then O / l and lse = m + log l
+      ok = mbar_wait(smem_u32(&bars.o_done[s]), 0, abortp, a.status) && ok;
+      fence_after_sync();
+      if (__all_sync(0xffffffffu, ok && !*abortp)) {
+        Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
+        const float inv = 1.f / lr;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32_sync(lane_addr + colO + c * 32, reinterpret_cast<uint32_t*>(o));
+          if (valid) store_row<Tout>(orow + c * 32, o, inv);
+        }
+        if (valid) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m_used + log2f(l)) * kLn2;
+        if (a.counts != nullptr && r == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = nret;
+      }
+      fence_before_sync();
     }
-    fence_before_sync();
   }
 
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 3) {
     fence_after_sync();
     tmem_dealloc<512>(tmem);
   }
@@ -388,7 +489,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches) {
       !encode_bshd_map(&mv, a.v, a.B, a.Lk, a.Hkv, kD, kBlk))
     return cudaErrorInvalidValue;
   const int tr = (a.Lq + kBlk - 1) / kBlk;
-  dim3 grid(a.Hq * a.B, tr);
+  dim3 grid(a.Hq * a.B, (tr + 1) / 2);
   ++*launches;
   cudaError_t e;
   if (a.out_dt == kBF16) {

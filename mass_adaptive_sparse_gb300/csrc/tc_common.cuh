@@ -84,6 +84,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Wait for an issued TMA copy to land before the CTA exits, whether or not
+// another role has aborted (a copy into shared memory always completes); still
+// bounded by kWaitLimitNs.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, 1);          // kStatusWaitTimeout
+      return;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
