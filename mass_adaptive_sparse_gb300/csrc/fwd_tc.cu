@@ -103,8 +103,10 @@ __device__ __forceinline__ void mask_cols(uint32_t* sr, int last) {
 }
 
 // 64 raw scores -> 32 packed bf16 pairs of P = exp2(S * scale - m) in sr[0..31];
-// acc sums P exactly, accr sums P as rounded to bf16 (two lanes per register).
-__device__ __forceinline__ void exp_pack(uint32_t* sr, uint64_t nsc2, uint64_t nm2, uint64_t& acc, uint64_t& accr) {
+// acc sums P exactly (two lanes per register), r0 / r1 sum the even / odd
+// columns' P as rounded to bf16.
+__device__ __forceinline__ void exp_pack(uint32_t* sr, uint64_t nsc2, uint64_t nm2, uint64_t& acc, float& r0,
+                                         float& r1) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     float e0, e1;
@@ -112,7 +114,7 @@ __device__ __forceinline__ void exp_pack(uint32_t* sr, uint64_t nsc2, uint64_t n
     const float p0 = ex2(e0), p1 = ex2(e1);
     const uint32_t w = pack_bf16(p0, p1);
     acc = add2(acc, f2(p0, p1));
-    accr = add2(accr, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+    add_bf16x2(r0, r1, w);
     sr[c] = w;
   }
 }
@@ -388,10 +390,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           if (!interior) mask_cols(sr, cmax - 64 * hf);
           // row max over legal keys (raw dot products; the scale is positive)
 #pragma unroll
-          for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
+          for (int c = 0; c < 64; c += 2)
+            mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
         }
-        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mraw = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         const float mt = mraw * a.scale_log2;
         const bool has = valid && lim >= j * kBlk;
         const int keep_row = has && (!test || l == 0.f || !(mt - m_used - lg2(l) < thr));
@@ -413,21 +415,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t nsc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-mref, -mref);
-        uint64_t acc = f2(0.f, 0.f), accr = f2(0.f, 0.f);
+        uint64_t acc = f2(0.f, 0.f);
+        float r0 = 0.f, r1 = 0.f;
         // P = exp2(S * scale - m_ref) as bf16 pairs; P of keys 64-127 goes over
         // the (consumed) scores of keys 64-95, P of keys 0-63 over keys 0-31
-        exp_pack(sr, nsc2, nm2, acc, accr);
+        exp_pack(sr, nsc2, nm2, acc, r0, r1);
         tmem_st32(lane_addr + colS + 64, sr);
         tmem_ld64_sync(lane_addr + colS, sr);
         if (!interior) mask_cols(sr, cmax);
-        exp_pack(sr, nsc2, nm2, acc, accr);
+        exp_pack(sr, nsc2, nm2, acc, r0, r1);
         float rowsum, rowsum_r;
         {
           float x0, x1;
           f2_split(acc, x0, x1);
           rowsum = x0 + x1;
-          f2_split(accr, x0, x1);
-          rowsum_r = x0 + x1;
+          rowsum_r = r0 + r1;
         }
         // O rescale when the reference max moved.  The slot's previous P V is
         // complete: it was issued before the Q K^T whose completion s_full reported.

@@ -319,6 +319,22 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// acc + the two bf16 halves of a packed pair, each widened exactly
+// (mixed-precision adds: no separate unpacking of the halves).
+__device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_t w) {
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n"
+      "add.rn.f32.bf16 %0, lo, %0;\n"
+      "add.rn.f32.bf16 %1, hi, %1; }"
+      : "+f"(acc_lo), "+f"(acc_hi) : "r"(w));
+}
+
 // Named barrier among `count` threads; the vote form returns the OR of `pred`.
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
