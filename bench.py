@@ -49,7 +49,8 @@ def _args():
     p.add_argument("--no-dense", action="store_true", help="skip the tau = 0 comparison loop")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-32k", action="store_true", help="skip the 32K prefill timing (128k workload)")
+    p.add_argument("--no-32k", action="store_true",
+                   help="skip the secondary timings (32K prefill, per-head decode)")
     p.add_argument("--sample-seconds", type=float, default=15.0)
     return p.parse_args()
 
@@ -550,6 +551,36 @@ def main():
             "bwd": {"ms": b1, "tflops": bwd_flops(c32, kb3) / b1 / 1e9, "kept_fraction": kb3 / u3["legal_tiles"]},
             "dense": {"fwd_ms": f0, "bwd_ms": b0, "speedup_fwd": f0 / f1, "speedup_bwd": b0 / b1}}}
         del e, flush
+
+    # --- the decode workload with each query head deciding alone (same kernels) ---
+    if not args.no_32k:
+        T_d = -(-dc.N // dc.block)
+        cdh = torch.zeros((dc.B, dc.H, dc.num_splits), dtype=torch.int32, device=dev)
+        mdh = torch.zeros((dc.B, dc.H, T_d), dtype=torch.uint8, device=dev)
+
+        def dech(t):
+            api.mala_decode_per_head(d["qd"], d["kc"], d["vc"], d["od"], d["lsed"], d["ws_d"], block=dc.block,
+                                     num_splits=dc.num_splits, tau=t, retained_counts=cdh, tile_mask=mdh)
+
+        for _ in range(max(3, args.warmup)):
+            dech(tau)
+        barrier()
+        evh = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evh[0].record(stream)
+        for s_ in range(args.steps):
+            dech(tau)
+            evh[s_ + 1].record(stream)
+        barrier()
+        us_h = max_over_ranks(statistics.mean(evh[i].elapsed_time(evh[i + 1]) for i in range(args.steps))) * 1e3
+        grp = dc.H // dc.Hkv
+        v_tiles = int(mdh.view(dc.B, dc.Hkv, grp, T_d).amax(dim=2).sum().item())   # V read when any head keeps
+        db_h = decode_bytes(dc, v_tiles)
+        secondary = secondary or {}
+        secondary["decode_per_head"] = {
+            "what": "decode_128k with each query head deciding alone (mala_decode_per_head)",
+            "us_per_token": us_h, "gbs": db_h / (us_h * 1e-3) / 1e6,
+            "kept_fraction_heads": int(cdh.sum().item()) / (dc.B * dc.H * T_d),
+            "v_tiles_read": v_tiles, "tiles": dc.B * dc.Hkv * T_d}
 
     cpu = None
     if pool is not None:

@@ -165,6 +165,27 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
                         int32_t* retained_counts, uint8_t* tile_mask, void* stream);
 
 /*
+ * MALA split-KV decode with per-head decisions (§2.2 states the skip rule per
+ * query block; here each query head is its own one-row block).
+ *
+ * Same arguments, layouts, workspace and errors as mala_decode, and the same
+ * split partition, order and merge.  The difference is who decides: each query
+ * head tests every tile against its own (m, l) and log(tau / cache_len), and
+ * a head that skips a tile leaves its (m, l, u) unchanged.  A tile's K is
+ * always read; its V is read when any head of the KV group keeps it, since
+ * the heads share it.  tau = 0 gives the same dense result as mala_decode.
+ *
+ *  retained_counts: [batch, heads_q, num_splits]   tiles each query head kept per split
+ *  tile_mask:       [batch, heads_q, ceil(cache_len / block_k)]
+ */
+mala_status mala_decode_per_head(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                 float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                                 int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                                 int num_splits, float tau, float softmax_scale,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/*
  * Variable-length MALA split-KV decode: mala_decode over a batch whose
  * sequences hold different numbers of cached tokens (App. A.1; §2.1 counts
  * L per query, and a decoding query's L is its own cache length, current

@@ -23,8 +23,8 @@ MALA_BF16, MALA_FP32 = 0, 1
 STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3: "MALA_ERR_WORKSPACE",
           4: "MALA_ERR_CUDA", 5: "MALA_ERR_TIMEOUT"}
 EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bwd",
-           "mala_decode_workspace_size", "mala_decode", "mala_decode_varlen", "mala_decode_noalloc",
-           "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
+           "mala_decode_workspace_size", "mala_decode", "mala_decode_per_head", "mala_decode_varlen",
+           "mala_decode_noalloc", "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
            "mala_last_cuda_error", "mala_cuda_error_string")
 
 
@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.mala_decode_workspace_size.argtypes = [_i] * 4
         L.mala_decode.restype = _i
         L.mala_decode.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
+        L.mala_decode_per_head.restype = _i
+        L.mala_decode_per_head.argtypes = [_vp] * 5 + [_i] * 5 + [_i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
         L.mala_decode_varlen.restype = _i
         L.mala_decode_varlen.argtypes = [_vp] * 6 + [_i] * 9 + [_f, _f, _vp, _sz, _vp, _vp, _vp]
         L.mala_decode_noalloc.restype = _i
@@ -157,6 +159,18 @@ def mala_decode(q, k_cache, v_cache, o, lse, workspace, *, block=128, num_splits
         _stream(stream)))
 
 
+def mala_decode_per_head(q, k_cache, v_cache, o, lse, workspace, *, block=128, num_splits=16, tau=1.0,
+                         softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
+    """mala_decode with each query head deciding alone; counts / mask per query head."""
+    B, Hq, D = q.shape
+    N, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _check("mala_decode_per_head", lib().mala_decode_per_head(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, N, Hq, Hkv, D, _dt(q), _dt(o),
+        block, num_splits, float(tau), _scale(D, softmax_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(retained_counts), _ptr(tile_mask),
+        _stream(stream)))
+
+
 def mala_decode_varlen(q, k_cache, v_cache, o, lse, cache_lens, workspace, *, block=128, num_splits=16,
                        tau=1.0, softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
     """mala_decode with per-sequence cache lengths (int32 CUDA tensor [B]) over
@@ -243,9 +257,10 @@ def backward(q, k, v, o, do, lse, tau=1.0, *, causal=True, block=128, softmax_sc
 
 
 def decode(q, k_cache, v_cache, tau=1.0, *, block=128, num_splits=16, softmax_scale=None,
-           out_dtype=None, counts=False, mask=False, cache_lens=None, stream=None):
+           out_dtype=None, counts=False, mask=False, cache_lens=None, per_head=False, stream=None):
     """Returns (o, lse, info).  `cache_lens` (int32 CUDA tensor [B]) selects
-    the variable-length decode over caches padded to k_cache.shape[1]."""
+    the variable-length decode over caches padded to k_cache.shape[1];
+    `per_head` lets each query head decide alone (counts / mask per query head)."""
     B, Hq, D = q.shape
     N, Hkv = k_cache.shape[1], k_cache.shape[2]
     dev = q.device
@@ -253,11 +268,18 @@ def decode(q, k_cache, v_cache, tau=1.0, *, block=128, num_splits=16, softmax_sc
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     ws = torch.empty(max(256, mala_decode_workspace_size(B, Hq, D, num_splits)), dtype=torch.uint8, device=dev)
     info = {}
+    if per_head and cache_lens is not None:
+        raise ValueError("per_head and cache_lens are separate entry points")
+    rows = Hq if per_head else Hkv
     if counts:
-        info["counts"] = torch.zeros((B, Hkv, num_splits), dtype=torch.int32, device=dev)
+        info["counts"] = torch.zeros((B, rows, num_splits), dtype=torch.int32, device=dev)
     if mask:
-        info["mask"] = torch.zeros((B, Hkv, _ntiles(N, block)), dtype=torch.uint8, device=dev)
-    if cache_lens is None:
+        info["mask"] = torch.zeros((B, rows, _ntiles(N, block)), dtype=torch.uint8, device=dev)
+    if per_head:
+        mala_decode_per_head(q, k_cache, v_cache, o, lse, ws, block=block, num_splits=num_splits, tau=tau,
+                             softmax_scale=softmax_scale, retained_counts=info.get("counts"),
+                             tile_mask=info.get("mask"), stream=stream)
+    elif cache_lens is None:
         mala_decode(q, k_cache, v_cache, o, lse, ws, block=block, num_splits=num_splits, tau=tau,
                     softmax_scale=softmax_scale, retained_counts=info.get("counts"),
                     tile_mask=info.get("mask"), stream=stream)

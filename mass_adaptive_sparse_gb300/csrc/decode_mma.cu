@@ -6,8 +6,11 @@
 // the test of Eq. (3) keeps.  Each split starts from its own empty (m, l),
 // visits its tiles newest to oldest and tests against L = N (the full
 // context).  The G query heads sharing a KV head form the query block: a tile
-// is kept if any of them keeps it.  The split writes (m, l, l_rounded, u) for
-// the exact merge of "Why exact attention does not need a quadratic matrix".
+// is kept if any of them keeps it.  In the per-head variant each query head
+// decides for itself: V is loaded if any head keeps the tile, and a head that
+// skips it takes P = 0 and keeps its (m, l).  The split writes
+// (m, l, l_rounded, u) for the exact merge of "Why exact attention does not
+// need a quadratic matrix".
 //
 // One CTA of 288 threads per (KV head, split, sequence):
 //   warp 8     TMA producer: K tiles, 3-stage ring, running ahead.
@@ -214,7 +217,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
   float m_g = -INFINITY;                 // reference max of head g
   float lw0 = 0.f, lw1 = 0.f;            // this warp's partial sums for heads 2cq, 2cq+1 (exact)
   float lr0 = 0.f, lr1 = 0.f;            // the same sums of P as rounded to bf16
-  int nret = 0, kept = 0;
+  int nret = 0, kept = 0, kept_g = 0;    // tiles kept by the group / by head g (lane g)
   bool ok = true;
 
   for (int t = 0; t < ntiles; ++t) {
@@ -272,9 +275,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     const float lt = (xl[t & 1][0][g] + xl[t & 1][1][g]) + (xl[t & 1][2][g] + xl[t & 1][3][g]);
     const bool keep_g = g < G && (lt == 0.f || !(tm - m_g - lg2(lt) < thr));
     const bool keep = !test || __any_sync(0xffffffffu, keep_g);
-    if (a.mask != nullptr && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
+    // head g's own decision: in the group variant every head follows the group
+    const bool own_g = a.per_head ? (!test || keep_g) : keep;
+    if (a.mask != nullptr) {
+      if (!a.per_head && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
+      if (a.per_head && tid < G) a.mask[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * Tmax + j] = own_g ? 1 : 0;
+    }
     if (!keep) continue;
     ++kept;
+    kept_g += own_g ? 1 : 0;
     const int vs = nret % kNV;
     // the slot (P and V) is free once the P V of kept tile nret - kNV is done
     if (nret >= kNV) ok = ok && mbar_wait(smem_u32(&bars.slot_empty[vs]), ((nret / kNV) - 1) & 1, abortp, a.status);
@@ -287,7 +296,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     }
     // lazily moved reference max (lane g), broadcast for this thread's heads 2cq, 2cq+1
     float alpha_g = 1.f;
-    if (tm > m_g + kRescale) {
+    if (own_g && tm > m_g + kRescale) {
       alpha_g = (m_g == -INFINITY) ? 0.f : ex2(m_g - tm);
       m_g = tm;
     }
@@ -295,14 +304,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     const float al0 = __shfl_sync(0xffffffffu, alpha_g, 2 * cq), al1 = __shfl_sync(0xffffffffu, alpha_g, 2 * cq + 1);
     const float mr0 = m0 == -INFINITY ? 0.f : m0;
     const float mr1 = m1 == -INFINITY ? 0.f : m1;
+    // a head that skips this tile contributes P = 0 (its (m, l) stay as they are)
+    const bool k0 = __shfl_sync(0xffffffffu, own_g, 2 * cq), k1 = __shfl_sync(0xffffffffu, own_g, 2 * cq + 1);
     float se0 = 0.f, se1 = 0.f, sr0 = 0.f, sr1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
         const int key = 32 * warp + 16 * mt + gq + 8 * hrow;
-        const float p0 = ex2(acc[mt][2 * hrow] - mr0);
-        const float p1 = ex2(acc[mt][2 * hrow + 1] - mr1);
+        const float p0 = k0 ? ex2(acc[mt][2 * hrow] - mr0) : 0.f;
+        const float p1 = k1 ? ex2(acc[mt][2 * hrow + 1] - mr1) : 0.f;
         const uint32_t w = pack_bf16(p0, p1);
         se0 += p0; se1 += p1;
         sr0 += __uint_as_float(w << 16);
@@ -346,8 +357,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     rec[2] = (xlr[0][lane] + xlr[1][lane]) + (xlr[2][lane] + xlr[3][lane]);
     rec[3] = 0.f;
   }
-  if (a.counts != nullptr && tid == 0 && !*abortp)
-    a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+  if (a.counts != nullptr && !*abortp) {
+    if (!a.per_head && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+    if (a.per_head && tid < G) a.counts[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * a.splits + sp] = kept_g;
+  }
   named_sync(2, 256);
   // V loads issued but never consumed (abort path) must land before exit; these
   // waits ignore the abort flag (they are still bounded in time)

@@ -130,7 +130,7 @@ mala_status run_decode(const void* q, const void* k_cache, const void* v_cache, 
                        const int32_t* cache_lens, int batch, int cache_len, int heads_q, int heads_kv,
                        int head_dim, int in_dtype, int out_dtype, int block_k, int num_splits, float tau,
                        float softmax_scale, float* partial, int32_t* retained_counts, uint8_t* tile_mask,
-                       int* status, void* stream) {
+                       int* status, void* stream, int per_head = 0) {
   DecArgs a{};
   a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
   a.B = batch; a.N = cache_len; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
@@ -139,6 +139,7 @@ mala_status run_decode(const void* q, const void* k_cache, const void* v_cache, 
   a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
   a.scale_log2 = softmax_scale * kLog2e;
   a.partial = partial;
+  a.per_head = per_head;
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
@@ -264,6 +265,24 @@ mala_status mala_decode(const void* q, const void* k_cache, const void* v_cache,
   return run_decode(q, k_cache, v_cache, o, lse, nullptr, batch, cache_len, heads_q, heads_kv, head_dim, in_dtype,
                     out_dtype, block_k, num_splits, tau, softmax_scale, static_cast<float*>(workspace),
                     retained_counts, tile_mask, status, stream);
+}
+
+mala_status mala_decode_per_head(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                 float* lse, int batch, int cache_len, int heads_q, int heads_kv,
+                                 int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int block_k,
+                                 int num_splits, float tau, float softmax_scale,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  const mala_status c = check_decode(q, k_cache, v_cache, o, lse, batch, cache_len, heads_q, heads_kv, head_dim,
+                                     in_dtype, out_dtype, block_k, num_splits, tau, softmax_scale);
+  if (c != MALA_OK) return c;
+  if (!workspace_ok(workspace, workspace_bytes, mala_decode_workspace_size(batch, heads_q, head_dim, num_splits)))
+    return MALA_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  return run_decode(q, k_cache, v_cache, o, lse, nullptr, batch, cache_len, heads_q, heads_kv, head_dim, in_dtype,
+                    out_dtype, block_k, num_splits, tau, softmax_scale, static_cast<float*>(workspace),
+                    retained_counts, tile_mask, status, stream, /*per_head=*/1);
 }
 
 mala_status mala_decode_varlen(const void* q, const void* k_cache, const void* v_cache, void* o,

@@ -54,8 +54,9 @@ struct DecArgs {
   float tau, log2_tau, scale_log2;
   float* partial;       // workspace: [splits, B, Hq, D + 4] = (m, l, l_rounded, 0, u[D]), m in log2 units;
                         // l sums P exactly, l_rounded sums P as rounded for the P V product
-  int32_t* counts;      // [B, Hkv, splits] or null
-  uint8_t* mask;        // [B, Hkv, T] or null
+  int per_head;         // 0: the KV head's query heads decide together; 1: each query head alone
+  int32_t* counts;      // [B, Hkv, splits] ([B, Hq, splits] per head) or null
+  uint8_t* mask;        // [B, Hkv, T] ([B, Hq, T] per head) or null
   int* status;
 };
 

@@ -315,7 +315,9 @@ bwd_simt_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------------------
 // Split-KV decode: one CTA of 128 threads per (split, KV head, batch); the G
-// query heads of the group form the query block.  Writes (m, l, u) per head.
+// query heads of the group form the query block (or, per head, each query head
+// decides alone: a head that skips a kept tile takes P = 0 and keeps its
+// (m, l)).  Writes (m, l, u) per head.
 // ---------------------------------------------------------------------------
 template <typename Tin, int D, int G, int BK>
 __global__ void __launch_bounds__(128)
@@ -349,6 +351,8 @@ decode_split_simt_kernel(const DecArgs a) {
 #pragma unroll
   for (int g = 0; g < G; ++g) { m[g] = -INFINITY; l[g] = 0.f; u[g] = 0.f; }
   int kept = 0;
+  __shared__ int kept_h[G];             // tiles kept by each head (per-head variant)
+  if (tid < G) kept_h[tid] = 0;
 
   for (int j = t1 - 1; j >= t0; --j) {
     const int k0 = j * BK;
@@ -381,19 +385,29 @@ decode_split_simt_kernel(const DecArgs a) {
     }
     __syncthreads();
     float mt[G];
-    bool keep = !test;
+    uint32_t own = 0;                     // bit g: head g keeps the tile
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float x = red[g][0];
 #pragma unroll
       for (int w = 1; w < NW; ++w) x = fmaxf(x, red[g][w]);
       mt[g] = x;
-      if (test && (l[g] == 0.f || !(x - m[g] - log2f(l[g]) < thr))) keep = true;
+      if (!test || l[g] == 0.f || !(x - m[g] - log2f(l[g]) < thr)) own |= 1u << g;
     }
-    if (a.mask != nullptr && tid == 0)
-      a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
+    const bool keep = own != 0;
+    if (!a.per_head && keep) own = (1u << G) - 1u;   // group: every head follows the group
+    if (a.mask != nullptr && tid == 0) {
+      if (a.per_head) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          a.mask[(static_cast<size_t>(b) * a.Hq + hk * G + g) * Tmax + j] = (own >> g) & 1u;
+      } else {
+        a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
+      }
+    }
     if (!keep) continue;
     ++kept;
+    if (tid < G) kept_h[tid] += (own >> tid) & 1u;
     for (int idx = tid; idx < BK * D; idx += NT) {
       const int kr = idx / D, c = idx % D, key = k0 + kr;
       Vs[kr][c] = key < n_b ? ld(vg + ((static_cast<size_t>(b) * a.N + key) * a.Hkv + hk) * D + c) : 0.f;
@@ -401,15 +415,16 @@ decode_split_simt_kernel(const DecArgs a) {
     float mnew[G], alpha[G], psum[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      mnew[g] = fmaxf(m[g], mt[g]);
-      alpha[g] = l[g] > 0.f ? exp2f(m[g] - mnew[g]) : 1.f;
+      const bool og = (own >> g) & 1u;
+      mnew[g] = og ? fmaxf(m[g], mt[g]) : m[g];
+      alpha[g] = (og && l[g] > 0.f) ? exp2f(m[g] - mnew[g]) : 1.f;
       psum[g] = 0.f;
     }
     __syncthreads();   // red[] reads above and Ps writes below; Vs complete
     for (int kr = tid; kr < BK; kr += NT) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float p = exp2f(Ps[g][kr] - mnew[g]);
+        const float p = ((own >> g) & 1u) ? exp2f(Ps[g][kr] - mnew[g]) : 0.f;
         Ps[g][kr] = p;
         psum[g] += p;
       }
@@ -447,7 +462,14 @@ decode_split_simt_kernel(const DecArgs a) {
       pp[4 + c] = u[g];
     }
   }
-  if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+  if (a.counts != nullptr && tid == 0) {
+    if (a.per_head) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) a.counts[(static_cast<size_t>(b) * a.Hq + hk * G + g) * a.splits + sp] = kept_h[g];
+    } else {
+      a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+    }
+  }
 }
 
 // Exact merge of the splits' (m, l, u): one CTA per (query head, batch).

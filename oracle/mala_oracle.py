@@ -44,7 +44,8 @@ __all__ = [
     "visible_key_counts", "dense_attention", "dense_attention_grads",
     "restricted_attention", "mala_forward", "mala_backward",
     "block_summary", "merge_summaries", "mala_decode",
-    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd", "mala_decode_varlen_bhd",
+    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd", "mala_decode_per_head_bhd",
+    "mala_decode_varlen_bhd",
     "omitted_mass", "BORDERLINE_REL",
 ]
 
@@ -463,6 +464,30 @@ def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=Non
             lse[b, hk * grp:(hk + 1) * grp] = r.lse
             retained[b, hk] = r.retained
             margin[b, hk] = r.margin
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+
+
+def mala_decode_per_head_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None):
+    """Per-head decode: the skip rule of §2.2 with each query head as its own
+    one-row query block, i.e. ``mala_decode`` on each head alone against its
+    KV head (same splits, order and merge).  q [B, Hq, d], caches
+    [B, N, Hkv, d] -> o [B, Hq, d], lse [B, Hq], retained/margin [B, Hq, T]."""
+    bsz, hq, d = q.shape
+    n, hkv = k_cache.shape[1], k_cache.shape[2]
+    grp = hq // hkv
+    t = -(-n // bk)
+    o = np.zeros((bsz, hq, v_cache.shape[3]))
+    lse = np.full((bsz, hq), np.nan)
+    retained = np.zeros((bsz, hq, t), dtype=bool)
+    margin = np.full((bsz, hq, t), np.nan)
+    for b in (range(bsz) if batches is None else batches):
+        for h in range(hq):
+            r = mala_decode(q[b, h:h + 1], k_cache[b, :, h // grp], v_cache[b, :, h // grp],
+                            scale, tau, bk, num_splits)
+            o[b, h] = r.o[0]
+            lse[b, h] = r.lse[0]
+            retained[b, h] = r.retained
+            margin[b, h] = r.margin
     return {"o": o, "lse": lse, "retained": retained, "margin": margin}
 
 

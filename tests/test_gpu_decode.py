@@ -13,10 +13,11 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None, lens=None):
+def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None, lens=None, per_head=False):
     """Decode on the GPU and compare with the oracle; `lens` (one cache length
     per sequence, each in [1, N]) selects the variable-length entry point over
-    caches padded to N."""
+    caches padded to N, `per_head` the entry point whose query heads decide
+    alone (masks and counts per query head)."""
     x = synthetic.decode_inputs(cfg, N=N, B=B, seed=seed)
     q, k, v = x["q"], x["k"], x["v"]
     if d is not None:
@@ -27,18 +28,23 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
     scale = 1 / math.sqrt(D)
     lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
     o, lse, info = api.decode(q.cuda(), k.cuda(), v.cuda(), tau, block=block, num_splits=splits,
-                              counts=True, mask=True, cache_lens=lens_t)
+                              counts=True, mask=True, cache_lens=lens_t, per_head=per_head)
     torch.cuda.synchronize()
     assert api.mala_device_status() == 0
     batches = list(range(B)) if batches is None else batches
     q64, k64, v64 = (parity.to64(t) for t in (q, k, v))
-    if lens is None:
+    if per_head:
+        ref = orc.mala_decode_per_head_bhd(q64, k64, v64, scale, tau, block, splits, batches=batches)
+    elif lens is None:
         ref = orc.mala_decode_bhd(q64, k64, v64, scale, tau, block, splits, batches=batches)
     else:
         ref = orc.mala_decode_varlen_bhd(q64, k64, v64, lens, scale, tau, block, splits, batches=batches)
     go, glse, gmask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
     Hq, Hkv = q.shape[1], k.shape[2]
     grp = Hq // Hkv
+    # a decision row is a KV head's group of query heads, or one query head
+    rows = [(h, slice(h, h + 1), h // grp) for h in range(Hq)] if per_head else \
+        [(hk, slice(hk * grp, (hk + 1) * grp), hk) for hk in range(Hkv)]
     fp32 = q.dtype == torch.float32
     ok = np.zeros((B, Hq), bool)
     flipped = 0
@@ -47,11 +53,10 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
         n_b = N if lens is None else lens[b]
         T = -(-n_b // block)
         per = -(-T // splits)
-        for hk in range(Hkv):
-            diff = gmask[b, hk, :T].astype(bool) != ref["retained"][b, hk, :T]
-            hs = slice(hk * grp, (hk + 1) * grp)
+        for row, hs, hk in rows:
+            diff = gmask[b, row, :T].astype(bool) != ref["retained"][b, row, :T]
             for sp in range(splits):
-                np.testing.assert_array_equal(counts[b, hk, sp], gmask[b, hk, sp * per:min(T, (sp + 1) * per)].sum())
+                np.testing.assert_array_equal(counts[b, row, sp], gmask[b, row, sp * per:min(T, (sp + 1) * per)].sum())
             if not diff.any():
                 ok[b, hs] = True
                 continue
@@ -59,13 +64,14 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
             for sp in range(splits):
                 idx = [j for j in range(min(T, (sp + 1) * per) - 1, sp * per - 1, -1) if diff[j]]
                 if idx:
-                    assert parity.is_borderline(ref["margin"][b, hk, idx[0]])
+                    assert parity.is_borderline(ref["margin"][b, row, idx[0]])
             flipped += 1
-            keep = gmask[b, hk, :T].astype(bool)[None, :]
+            keep = gmask[b, row, :T].astype(bool)[None, :]
+            nrow = hs.stop - hs.start
             o_r, lse_r = orc.restricted_attention(q64[b, hs], k64[b, :n_b, hk], v64[b, :n_b, hk], scale, keep,
-                                                  grp, block, causal=False)
+                                                  nrow, block, causal=False)
             parity.check_close("o (flipped)", go[b, hs], o_r, q.dtype, fp32=fp32)
-    assert flipped <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * Hkv)
+    assert flipped <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * len(rows))
     m = parity.check_close("o", go[ok], ref["o"][ok], q.dtype, fp32=fp32)
     assert np.abs(glse[ok] - ref["lse"][ok]).max() <= parity.LSE_ABS
     return m, gmask
@@ -147,3 +153,30 @@ def test_decode_varlen_rejects_bad_lengths_per_sequence():
     for b in (0, 3):
         parity.check_close("o", go[b], ref["o"][b], q.dtype)
         assert np.abs(glse[b] - ref["lse"][b]).max() <= parity.LSE_ABS
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+@pytest.mark.parametrize("tau", [0.0, 1.0, 16.0])
+def test_decode_per_head_small_bf16(splits, tau):
+    """Each query head decides alone (tensor-core split kernel, group of 4)."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 1000, 2, tau, splits, 128, 11, per_head=True)
+
+
+@pytest.mark.parametrize("H,Hkv", [(16, 2), (8, 4)])
+def test_decode_per_head_group_sizes(H, Hkv):
+    cfg = dataclasses.replace(synthetic.CONFIGS["decode_128k"], H=H, Hkv=Hkv)
+    _check(cfg, 1500, 2, 1.0, 4, 128, 43, per_head=True)
+
+
+def test_decode_per_head_fp32_d64():
+    """The CUDA-core split kernel (fp32, head_dim 64, 64-key tiles)."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, 777, 2, 4.0, 5, 64, 47, dtype=torch.float32, d=64, per_head=True)
+
+
+def test_decode_per_head_128k_full_size_sampled():
+    """Batch 8, 32 query heads over 8 KV heads, 131072-token cache, 16 splits,
+    each head deciding alone; sequences 1 and 6 compared with the oracle."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _check(cfg, cfg.N, cfg.B, 1.0, cfg.num_splits, cfg.block, cfg.seed, batches=[1, 6], per_head=True)

@@ -440,3 +440,78 @@ def test_decode_varlen_tau0_is_dense_over_each_prefix(lens, splits):
         o_ref, lse_ref = _sdpa(q[b], k[b, :n, 0], v[b, :n, 0], 0.25, causal=False)
         np.testing.assert_allclose(r["o"][b], o_ref, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(r["lse"][b], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Per-head decode: §2.2's rule with each query head as its own one-row block.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_per_head_tau0_is_dense(splits):
+    q = _rand((2, 4, 16), 101, 2.0)
+    k, v = _rand((2, 300, 2, 16), 102), _rand((2, 300, 2, 16), 103)
+    r = orc.mala_decode_per_head_bhd(q, k, v, 0.25, 0.0, 32, splits)
+    for b in range(2):
+        for h in range(4):
+            o_ref, lse_ref = _sdpa(q[b, h:h + 1], k[b, :, h // 2], v[b, :, h // 2], 0.25, causal=False)
+            np.testing.assert_allclose(r["o"][b, h], o_ref[0], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(r["lse"][b, h], lse_ref[0], rtol=1e-12)
+    assert r["retained"].all()
+
+
+def test_decode_per_head_single_split_equals_forward_on_one_row():
+    """With one split, each head's decode is Algorithm 1 on a one-row query
+    block seeing the whole cache (L = N), tiles newest first."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    x = synthetic.decode_inputs(cfg, N=1000, B=1, seed=5)
+    q = x["q"][:, 0:4].double().numpy()
+    kc, vc = x["k"][:, :, 0:1].double().numpy(), x["v"][:, :, 0:1].double().numpy()
+    scale = 1 / math.sqrt(128)
+    r = orc.mala_decode_per_head_bhd(q, kc, vc, scale, 1.0, 128, 1)
+    for h in range(4):
+        f = orc.mala_forward(q[0, h:h + 1], kc[0, :, 0], vc[0, :, 0], scale, 1.0, 1, 128, causal=False)
+        np.testing.assert_allclose(r["o"][0, h], f.o[0], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(r["lse"][0, h], f.lse[0], rtol=1e-13)
+        assert np.array_equal(r["retained"][0, h], f.retained[0])
+
+
+def test_decode_per_head_differs_from_group_closed_form():
+    """Two heads over one 100-token cache, 32-key tiles, one split, tau = 4,
+    L = 100.  Head 0 sees uniform scores (q = 0): it keeps the newest tile
+    (l = 0), then the next (ratio -log 4 >= log(4/100)), and skips the two
+    older ones (-log 36 < log(4/100)): output = mean of v over keys 64..99,
+    lse = log 36.  Head 1 sees the same zeros except one score of 9 at key 5:
+    it also keeps the oldest tile (9 - log 36 >= log(4/100)), so its output is
+    (sum of v over keys 0..31 and 64..99, key 5 weighted e^9) / (67 + e^9 - 1).
+    Deciding as a group, head 0 would have taken the oldest tile too."""
+    n, d = 100, 8
+    k = _rand((1, n, 1, d), 111)
+    k[0, :, 0, 0] = 0.0
+    k[0, 5, 0, 0] = 9.0
+    v = _rand((1, n, 1, d), 112)
+    q = np.zeros((1, 2, d))
+    q[0, 1, 0] = 1.0
+    r = orc.mala_decode_per_head_bhd(q, k, v, 1.0, 4.0, 32, 1)
+    assert r["retained"][0, 0].tolist() == [False, False, True, True]
+    assert r["retained"][0, 1].tolist() == [True, False, True, True]
+    np.testing.assert_allclose(r["o"][0, 0], v[0, 64:100, 0].mean(axis=0), rtol=1e-13)
+    np.testing.assert_allclose(r["lse"][0, 0], math.log(36.0), rtol=1e-13)
+    w = np.zeros(n)
+    w[0:32] = 1.0
+    w[64:100] = 1.0
+    w[5] = math.exp(9.0)
+    np.testing.assert_allclose(r["o"][0, 1], (w[:, None] * v[0, :, 0]).sum(0) / w.sum(), rtol=1e-12)
+    np.testing.assert_allclose(r["lse"][0, 1], math.log(w.sum()), rtol=1e-13)
+    g = orc.mala_decode_bhd(q, k, v, 1.0, 4.0, 32, 1)
+    assert g["retained"][0, 0].tolist() == [True, False, True, True]
+    np.testing.assert_allclose(g["o"][0, 0], v[0, list(range(32)) + list(range(64, 100)), 0].mean(axis=0),
+                               rtol=1e-12)
+
+
+def test_decode_per_head_with_single_head_groups_is_the_group_decode():
+    q = _rand((2, 3, 16), 121, 2.0)
+    k, v = _rand((2, 250, 3, 16), 122), _rand((2, 250, 3, 16), 123)
+    a = orc.mala_decode_per_head_bhd(q, k, v, 0.25, 2.0, 32, 3)
+    b = orc.mala_decode_bhd(q, k, v, 0.25, 2.0, 32, 3)
+    np.testing.assert_array_equal(a["retained"], b["retained"])
+    np.testing.assert_allclose(a["o"], b["o"], rtol=0, atol=0)
