@@ -130,6 +130,52 @@ mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* workspace, size_t workspace_bytes,
                      int32_t* retained_counts, uint8_t* tile_mask, void* stream);
 
+/*
+ * Variable-length prefill: mala_fwd / mala_bwd over a batch of sequences of
+ * different lengths packed along one token axis (§2.1 counts L_q per query
+ * row; each sequence is its own causal context).
+ *
+ * Sequence b holds the token rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1 and
+ * attends only within itself; each gives exactly what mala_fwd / mala_bwd
+ * give on that sequence alone (batch 1, seqlen_q = seqlen_k = its length).
+ *
+ *  q, o, dout, dq   [total_tokens, heads_q,  head_dim]
+ *  k, v, dk, dv     [total_tokens, heads_kv, head_dim]
+ *  lse              [heads_q, total_tokens]  (float)
+ *  cu_seqlens       [batch + 1] int32, device memory, 4-byte aligned, with
+ *                   0 <= cu_seqlens[b] <= cu_seqlens[b + 1] <= total_tokens
+ *                   and no sequence longer than max_seqlen (1 <= max_seqlen <= total_tokens)
+ *  retained_counts  mala_fwd_varlen: [batch, heads_q, ceil(max_seqlen / block_q)];
+ *                   mala_bwd_varlen: [batch, heads_q, ceil(max_seqlen / block_k)]
+ *  tile_mask        [batch, heads_q, T, T], T = ceil(max_seqlen / block): a
+ *                   sequence's entries past its own tiles are not written
+ *  workspace        mala_bwd_varlen: >= mala_bwd_varlen_workspace_size(...) bytes
+ * Everything else (dtypes, causal flag, tiles, tau, scale) as mala_fwd / mala_bwd.
+ * The bounds are read on the device: a sequence that breaks them sets bit 2
+ * of the device status word (mala_device_status) and is not computed (its
+ * outputs are not written); the other sequences are unaffected.  A null or
+ * misaligned cu_seqlens, or max_seqlen outside [1, total_tokens], returns
+ * MALA_ERR_INVALID_ARG.
+ */
+mala_status mala_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                            int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                            mala_dtype out_dtype, int causal, int block_q, int block_k, float tau,
+                            float softmax_scale, int32_t* retained_counts, uint8_t* tile_mask,
+                            void* stream);
+
+/* Bytes of device workspace mala_bwd_varlen needs for these sizes. */
+size_t mala_bwd_varlen_workspace_size(int total_tokens, int heads_q, int heads_kv, int head_dim,
+                                      mala_dtype in_dtype, mala_dtype grad_dtype);
+
+mala_status mala_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                            int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                            mala_dtype grad_dtype, int causal, int block_q, int block_k, float tau,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
 /* Bytes of device workspace mala_decode needs for these sizes. */
 size_t mala_decode_workspace_size(int batch, int heads_q, int head_dim, int num_splits);
 
@@ -254,7 +300,8 @@ size_t mala_decode_noalloc_max_floats(void);
  * Synchronise `stream`, then read and clear the device status word that the
  * kernels set.  Bits: 1 = a bounded on-chip wait expired (the kernel gave up
  * and its outputs are not valid); 2 = mala_decode_varlen read a sequence
- * length outside [1, max_cache_len].  *device_code receives the raw word
+ * length outside [1, max_cache_len], or mala_fwd_varlen / mala_bwd_varlen
+ * read sequence bounds that break their contract.  *device_code receives the raw word
  * (0 = no event).  Returns MALA_OK (word 0), MALA_ERR_TIMEOUT (bit 1 set),
  * MALA_ERR_INVALID_ARG (any other bit), or MALA_ERR_CUDA if synchronisation
  * failed.

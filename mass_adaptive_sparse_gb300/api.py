@@ -23,6 +23,7 @@ MALA_BF16, MALA_FP32 = 0, 1
 STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3: "MALA_ERR_WORKSPACE",
           4: "MALA_ERR_CUDA", 5: "MALA_ERR_TIMEOUT"}
 EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bwd",
+           "mala_fwd_varlen", "mala_bwd_varlen_workspace_size", "mala_bwd_varlen",
            "mala_decode_workspace_size", "mala_decode", "mala_decode_per_head", "mala_decode_varlen",
            "mala_decode_noalloc", "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
            "mala_last_cuda_error", "mala_cuda_error_string")
@@ -54,6 +55,12 @@ def lib() -> ctypes.CDLL:
         L.mala_bwd_workspace_size.argtypes = [_i] * 8
         L.mala_bwd.restype = _i
         L.mala_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_i, _i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
+        L.mala_fwd_varlen.restype = _i
+        L.mala_fwd_varlen.argtypes = [_vp] * 6 + [_i] * 6 + [_i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]
+        L.mala_bwd_varlen_workspace_size.restype = _sz
+        L.mala_bwd_varlen_workspace_size.argtypes = [_i] * 6
+        L.mala_bwd_varlen.restype = _i
+        L.mala_bwd_varlen.argtypes = [_vp] * 10 + [_i] * 6 + [_i, _i, _i, _i, _i, _f, _f, _vp, _sz, _vp, _vp, _vp]
         L.mala_decode_workspace_size.restype = _sz
         L.mala_decode_workspace_size.argtypes = [_i] * 4
         L.mala_decode.restype = _i
@@ -140,6 +147,45 @@ def mala_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, *, causal=True, block=1
     _check("mala_bwd", lib().mala_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         B, Lq, Lk, Hq, Hkv, D, _dt(q), _dt(dq), int(causal), block, block, float(tau),
+        _scale(D, softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(retained_counts), _ptr(tile_mask), _stream(stream)))
+
+
+def _check_cu(cu_seqlens, batch):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.shape != (batch + 1,) or not cu_seqlens.is_cuda:
+        raise ValueError("cu_seqlens must be an int32 CUDA tensor of shape [batch + 1]")
+
+
+def mala_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, *, causal=True, block=128, tau=1.0,
+                    softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
+    """Packed variable-length forward: q, o [total, Hq, D], k, v [total, Hkv, D],
+    lse [Hq, total]; sequence b is rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    _check_cu(cu_seqlens, B)
+    _check("mala_fwd_varlen", lib().mala_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B, T, int(max_seqlen), Hq, Hkv, D,
+        _dt(q), _dt(o), int(causal), block, block, float(tau), _scale(D, softmax_scale),
+        _ptr(retained_counts), _ptr(tile_mask), _stream(stream)))
+
+
+def mala_bwd_varlen_workspace_size(q, k, grad_dtype):
+    T, Hq, D = q.shape
+    return lib().mala_bwd_varlen_workspace_size(T, Hq, k.shape[1], D, _dt(q),
+                                                MALA_BF16 if grad_dtype == torch.bfloat16 else MALA_FP32)
+
+
+def mala_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, workspace, *, causal=True,
+                    block=128, tau=1.0, softmax_scale=None, retained_counts=None, tile_mask=None, stream=None):
+    """Packed variable-length backward (layouts as mala_fwd_varlen)."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    _check_cu(cu_seqlens, B)
+    _check("mala_bwd_varlen", lib().mala_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens),
+        B, T, int(max_seqlen), Hq, Hkv, D, _dt(q), _dt(dq), int(causal), block, block, float(tau),
         _scale(D, softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(retained_counts), _ptr(tile_mask), _stream(stream)))
 
@@ -253,6 +299,47 @@ def backward(q, k, v, o, do, lse, tau=1.0, *, causal=True, block=128, softmax_sc
     mala_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, causal=causal, block=block, tau=tau,
              softmax_scale=softmax_scale, retained_counts=info.get("counts"),
              tile_mask=info.get("mask"), stream=stream)
+    return dq, dk, dv, info
+
+
+def forward_varlen(q, k, v, cu_seqlens, max_seqlen, tau=1.0, *, causal=True, block=128, softmax_scale=None,
+                   out_dtype=None, counts=False, mask=False, stream=None):
+    """Packed variable-length forward; returns (o [total, Hq, D], lse [Hq, total], info)."""
+    T, Hq, D = q.shape
+    B = cu_seqlens.shape[0] - 1
+    o = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    t = _ntiles(max_seqlen, block)
+    info = {}
+    if counts:
+        info["counts"] = torch.zeros((B, Hq, t), dtype=torch.int32, device=q.device)
+    if mask:
+        info["mask"] = torch.zeros((B, Hq, t, t), dtype=torch.uint8, device=q.device)
+    mala_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal=causal, block=block, tau=tau,
+                    softmax_scale=softmax_scale, retained_counts=info.get("counts"), tile_mask=info.get("mask"),
+                    stream=stream)
+    return o, lse, info
+
+
+def backward_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, tau=1.0, *, causal=True, block=128,
+                    softmax_scale=None, grad_dtype=torch.float32, counts=False, mask=False, stream=None):
+    """Packed variable-length backward; returns (dq, dk, dv, info)."""
+    T, Hq, D = q.shape
+    B = cu_seqlens.shape[0] - 1
+    dev = q.device
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=dev)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=dev)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=dev)
+    ws = torch.empty(max(256, mala_bwd_varlen_workspace_size(q, k, grad_dtype)), dtype=torch.uint8, device=dev)
+    t = _ntiles(max_seqlen, block)
+    info = {}
+    if counts:
+        info["counts"] = torch.zeros((B, Hq, t), dtype=torch.int32, device=dev)
+    if mask:
+        info["mask"] = torch.zeros((B, Hq, t, t), dtype=torch.uint8, device=dev)
+    mala_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, ws, causal=causal, block=block,
+                    tau=tau, softmax_scale=softmax_scale, retained_counts=info.get("counts"),
+                    tile_mask=info.get("mask"), stream=stream)
     return dq, dk, dv, info
 
 

@@ -129,8 +129,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const int bh = blockIdx.x;
   const int hk = bh % a.Hkv, b = bh / a.Hkv;
   const int kb = blockIdx.y;                                   // small key blocks (most work) first
+  // this CTA's sequence: its lengths, first row and batch coordinate in the layout
+  const SeqSpan sq = seq_span(a, b);
+  const int Lq = sq.Lq, Lk = sq.Lk, row0 = sq.row0, bc = sq.bc;
   const int G = a.Hq / a.Hkv;
-  const int Tr = (a.Lq + kBlk - 1) / kBlk, Tc = (a.Lk + kBlk - 1) / kBlk;
+  const int Tr = (Lq + kBlk - 1) / kBlk, Tc = (Lk + kBlk - 1) / kBlk;
+  if (kb >= Tc) return;                  // past the sequence's key blocks (packed batches)
+  // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
+  const int mTr = a.cu ? (a.Lmax + kBlk - 1) / kBlk : Tr, mTc = a.cu ? mTr : Tc;
   const int ibot = a.causal ? kb : 0;
   const int ni = Tr - ibot;
   const int ntiles = G * ni;
@@ -166,10 +172,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       prefetch_tensormap(&mdo);
       const uint32_t kvf = smem_u32(&bars.kv_full);
       mbar_expect_tx(kvf, 2 * kTile);
-      tma_load_4d(sK, &mk, kvf, 0, hk, kb * kBlk, b);
-      tma_load_4d(sK + kHalf, &mk, kvf, 64, hk, kb * kBlk, b);
-      tma_load_4d(sV, &mv, kvf, 0, hk, kb * kBlk, b);
-      tma_load_4d(sV + kHalf, &mv, kvf, 64, hk, kb * kBlk, b);
+      tma_load_4d(sK, &mk, kvf, 0, hk, row0 + kb * kBlk, bc);
+      tma_load_4d(sK + kHalf, &mk, kvf, 64, hk, row0 + kb * kBlk, bc);
+      tma_load_4d(sV, &mv, kvf, 0, hk, row0 + kb * kBlk, bc);
+      tma_load_4d(sV + kHalf, &mv, kvf, 64, hk, row0 + kb * kBlk, bc);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1, n = t >> 1;
@@ -177,8 +183,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int h = hk * G + t / ni, i = ibot + t % ni;
         const uint32_t qf = smem_u32(&bars.q_full[s]);
         mbar_expect_tx(qf, kTile);
-        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, i * kBlk, b);
-        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, i * kBlk, b);
+        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row0 + i * kBlk, bc);
+        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row0 + i * kBlk, bc);
         ++issued;
       }
       mbar_wait(kvf, 0, abortp, a.status);
@@ -272,8 +278,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int r = tid & 127;                    // key row = TMEM lane
     const int cg = tid >> 7;                    // column group: queries / head dims [64cg, 64cg + 64)
     const int key = kb * kBlk + r;
-    const bool key_ok = key < a.Lk;
-    const bool keys_full = kb * kBlk + kBlk <= a.Lk;
+    const bool key_ok = key < Lk;
+    const bool keys_full = kb * kBlk + kBlk <= Lk;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool test = a.tau > 0.f;
     const float sl2 = a.scale_log2;
@@ -294,11 +300,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     auto fetch = [&](int t) {
       const int h = hk * G + t / ni, i = ibot + t % ni;
       const int q = i * kBlk + r;
-      if (q < a.Lq) {
-        const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.Lq + q;
+      if (q < Lq) {
+        const size_t off = (static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + q;
         n_lse = a.lse[off];
         n_d = a.delta[off];
-        n_thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(a.Lk))
+        n_thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(Lk))
                      : -INFINITY;
       } else {
         n_lse = 0.f; n_d = 0.f; n_thr = INFINITY;     // out of range: never kept
@@ -333,9 +339,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       if (tid == 0) {
         if (release) mbar_arrive(smem_u32(&bars.dq_free));
         // two bulk groups: the first (staged in the dS buffer) is waited for alone before dS is written
-        if (prev_q0 < a.Lq) tma_reduce_add_4d(&mdq, sDS, 0, prev_h, prev_q0, b);
+        // rows past the sequence add exact zeros (their dS columns are 0)
+        if (prev_q0 < Lq) tma_reduce_add_4d(&mdq, sDS, 0, prev_h, row0 + prev_q0, bc);
         bulk_commit();
-        if (prev_q0 + 64 < a.Lq) tma_reduce_add_4d(&mdq, sST, 0, prev_h, prev_q0 + 64, b);
+        if (prev_q0 + 64 < Lq) tma_reduce_add_4d(&mdq, sST, 0, prev_h, row0 + prev_q0 + 64, bc);
         bulk_commit();
       }
       return true;
@@ -359,7 +366,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       fence_after_sync();
       // Eq. (4): keep iff some valid entry has S - lse >= log(tau / L_q)
       const bool diag = a.causal && q0 == kb * kBlk;
-      const int qlim = a.Lq - q0;                 // query columns at or beyond this are out of range
+      const int qlim = Lq - q0;                   // query columns at or beyond this are out of range
       const int qmin = diag ? r : 0;              // causal: query >= key inside the diagonal tile
       const bool interior = !diag && qlim >= kBlk && keys_full;
       const float4* c4 = reinterpret_cast<const float4*>(&vec_c[64 * cg]);
@@ -391,11 +398,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       // an abort is caught at the vote after P^T is stored, or (skipped tiles)
       // by the next tile's waits, which return at once once the flag is up
       const int keep = named_vote_or(1, kMath, keep_row && ok);
-      uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + i) * Tc + kb : nullptr;
+      uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb : nullptr;
       if (tid == 0) {
         head_kept += keep;
         if (t % ni == ni - 1) {                   // last query block of this head
-          if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tc + kb] = head_kept;
+          if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTc + kb] = head_kept;
           head_kept = 0;
         }
       }
@@ -420,8 +427,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (ok) {
           const uint32_t df = smem_u32(&bars.do_full);
           mbar_expect_tx(df, kTile);
-          tma_load_4d(sDO, &mdo, df, 0, h, q0, b);
-          tma_load_4d(sDO + kHalf, &mdo, df, 64, h, q0, b);
+          tma_load_4d(sDO, &mdo, df, 0, h, row0 + q0, bc);
+          tma_load_4d(sDO + kHalf, &mdo, df, 64, h, row0 + q0, bc);
           ++do_issued;
         }
       }
@@ -522,7 +529,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (tid == 0) bulk_wait0();        // every reduce-add has landed before the CTA exits
     fence_after_sync();
     if (__all_sync(0xffffffffu, ok && !*abortp)) {
-      const size_t off = ((static_cast<size_t>(b) * a.Lk + (key_ok ? key : 0)) * a.Hkv + hk) * kD + 64 * cg;
+      const size_t off = ((static_cast<size_t>(bc) * a.Lk + row0 + (key_ok ? key : 0)) * a.Hkv + hk) * kD + 64 * cg;
       Tg* dvp = static_cast<Tg*>(a.dv) + off;
       Tg* dkp = static_cast<Tg*>(a.dk) + off;
 #pragma unroll
@@ -556,8 +563,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 // normal range), D = rowsum(O * dO), and a zeroed fp32 dQ accumulator.  One
 // warp per row; each lane converts 4 of the 128 elements.
 __global__ void bwd_tc_prep_kernel(const BwdArgs a, uint32_t* q16, uint32_t* k16, uint32_t* v16, uint32_t* do16) {
-  const size_t qrows = static_cast<size_t>(a.B) * a.Lq * a.Hq;
-  const size_t krows = static_cast<size_t>(a.B) * a.Lk * a.Hkv;
+  const size_t lb = a.cu ? 1 : a.B;       // a packed batch is one run of Lq rows
+  const size_t qrows = lb * a.Lq * a.Hq;
+  const size_t krows = lb * a.Lk * a.Hkv;
   const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (row < qrows) {
@@ -603,24 +611,25 @@ size_t bwd_tc_scratch_bytes(int B, int Lq, int Lk, int Hq, int Hkv, int D) {
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t s, int* launches) {
   // fp16 copies: q, dO [B, Lq, Hq, D] then k, v [B, Lk, Hkv, D] (two halves per 32-bit word)
+  const int lb = a.cu ? 1 : a.B;           // a packed batch is one run of Lq rows
   uint32_t* q16 = static_cast<uint32_t*>(a.scratch);
-  uint32_t* do16 = q16 + static_cast<size_t>(a.B) * a.Lq * a.Hq * kD / 2;
-  uint32_t* k16 = do16 + static_cast<size_t>(a.B) * a.Lq * a.Hq * kD / 2;
-  uint32_t* v16 = k16 + static_cast<size_t>(a.B) * a.Lk * a.Hkv * kD / 2;
-  const size_t rows = std::max(static_cast<size_t>(a.B) * a.Lq * a.Hq, static_cast<size_t>(a.B) * a.Lk * a.Hkv);
+  uint32_t* do16 = q16 + static_cast<size_t>(lb) * a.Lq * a.Hq * kD / 2;
+  uint32_t* k16 = do16 + static_cast<size_t>(lb) * a.Lq * a.Hq * kD / 2;
+  uint32_t* v16 = k16 + static_cast<size_t>(lb) * a.Lk * a.Hkv * kD / 2;
+  const size_t rows = std::max(static_cast<size_t>(lb) * a.Lq * a.Hq, static_cast<size_t>(lb) * a.Lk * a.Hkv);
   bwd_tc_prep_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, s>>>(a, q16, k16, v16, do16);
   ++*launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_bshd_map(&mq, q16, a.B, a.Lq, a.Hq, kD, kBlk, true) ||
-      !encode_bshd_map(&mdo, do16, a.B, a.Lq, a.Hq, kD, kBlk, true) ||
-      !encode_bshd_map(&mk, k16, a.B, a.Lk, a.Hkv, kD, kBlk, true) ||
-      !encode_bshd_map(&mv, v16, a.B, a.Lk, a.Hkv, kD, kBlk, true))
+  if (!encode_bshd_map(&mq, q16, lb, a.Lq, a.Hq, kD, kBlk, true) ||
+      !encode_bshd_map(&mdo, do16, lb, a.Lq, a.Hq, kD, kBlk, true) ||
+      !encode_bshd_map(&mk, k16, lb, a.Lk, a.Hkv, kD, kBlk, true) ||
+      !encode_bshd_map(&mv, v16, lb, a.Lk, a.Hkv, kD, kBlk, true))
     return cudaErrorInvalidValue;
   CUtensorMap mdq;
-  if (!encode_bshd_f32_map(&mdq, a.dq_acc, a.B, a.Lq, a.Hq, kD, 64)) return cudaErrorInvalidValue;
-  const int tc = (a.Lk + kBlk - 1) / kBlk;
+  if (!encode_bshd_f32_map(&mdq, a.dq_acc, lb, a.Lq, a.Hq, kD, 64)) return cudaErrorInvalidValue;
+  const int tc = ((a.cu ? a.Lmax : a.Lk) + kBlk - 1) / kBlk;
   dim3 grid(a.Hkv * a.B, tc);
   ++*launches;
   if (a.grad_dt == kBF16) {

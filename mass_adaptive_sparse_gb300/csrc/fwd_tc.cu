@@ -137,8 +137,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int bh = blockIdx.x;
   const int h = bh % a.Hq, b = bh / a.Hq;
-  const int Tr = (a.Lq + kBlk - 1) / kBlk, Tc = (a.Lk + kBlk - 1) / kBlk;
+  // this CTA's sequence: its lengths, first row and batch coordinate in the layout
+  const SeqSpan sq = seq_span(a, b);
+  const int Lq = sq.Lq, Lk = sq.Lk, row0 = sq.row0, bc = sq.bc;
+  const int Tr = (Lq + kBlk - 1) / kBlk, Tc = (Lk + kBlk - 1) / kBlk;
+  // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
+  const int mTr = a.cu ? (a.Lmax + kBlk - 1) / kBlk : Tr, mTc = a.cu ? mTr : Tc;
   const int pair = (Tr + 1) / 2 - 1 - static_cast<int>(blockIdx.y);   // heaviest pairs first
+  if (pair < 0) return;                  // past the sequence's query blocks (packed batches)
   const int nslots = (2 * pair + 1 < Tr) ? 2 : 1;
   const int hk = h / (a.Hq / a.Hkv);
   // top key block of each slot; the pair walks from the higher one down to 0
@@ -146,7 +152,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int qb = 2 * pair + s;
-    jtop_s[s] = a.causal ? min(Tc - 1, (min(a.Lq, qb * kBlk + kBlk) - 1) / kBlk) : Tc - 1;
+    jtop_s[s] = a.causal ? min(Tc - 1, (min(Lq, qb * kBlk + kBlk) - 1) / kBlk) : Tc - 1;
   }
   if (nslots == 1) jtop_s[1] = -1;
   const int jtop = max(jtop_s[0], jtop_s[1]);
@@ -192,19 +198,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const uint32_t qf = smem_u32(&bars.q_full);
       mbar_expect_tx(qf, kTile * nslots);
       for (int s = 0; s < nslots; ++s) {
-        const int row = (2 * pair + s) * kBlk;
-        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, b);
-        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, b);
+        const int row = row0 + (2 * pair + s) * kBlk;
+        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, bc);
+        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, bc);
       }
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % kNK, n = t / kNK;
         if (n > 0 && !mbar_wait(smem_u32(&bars.k_empty[st]), (n - 1) & 1, abortp, a.status)) break;
         const uint32_t kf = smem_u32(&bars.k_full[st]);
-        const int row = (jtop - t) * kBlk;
+        const int row = row0 + (jtop - t) * kBlk;
         mbar_expect_tx(kf, kTile);
-        tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, b);
-        tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, b);
+        tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, bc);
+        tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, bc);
         ++issued;
       }
       // every issued load lands before the CTA can finish
@@ -232,8 +238,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             if (ok) {
               const uint32_t vf = smem_u32(&bars.v_full[vs]);
               mbar_expect_tx(vf, kTile);
-              tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, (jtop - t) * kBlk, b);
-              tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, (jtop - t) * kBlk, b);
+              tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, row0 + (jtop - t) * kBlk, bc);
+              tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, row0 + (jtop - t) * kBlk, bc);
               load = true;
               armed = t;
             }
@@ -353,9 +359,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (s < nslots) {
       const int qb = 2 * pair + s;
       const int qrow = qb * kBlk + r;
-      const bool valid = qrow < a.Lq;
-      const int lim = a.causal ? min(qrow, a.Lk - 1) : a.Lk - 1;   // last legal key of this row
-      const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk));
+      const bool valid = qrow < Lq;
+      const int lim = a.causal ? min(qrow, Lk - 1) : Lk - 1;       // last legal key of this row
+      const float thr = a.log2_tau - log2f(a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(Lk));
       const bool test = a.tau > 0.f;
       const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
       const uint32_t colS = s * 128, colO = kColO + s * 128;
@@ -364,7 +370,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       float m_used = -INFINITY, l = 0.f, lr = 0.f;
       int nret = 0, it = 0;
       bool ok = true;
-      uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc : nullptr;
+      uint8_t* mask_row = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * mTr + qb) * mTc : nullptr;
       const int t0 = jtop - jtop_s[s];
 
       // After a timed-out wait the loop runs on without breaking (waits then
@@ -378,7 +384,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         // the max pass reads both, the exponent pass reuses the second half
         // still in registers and reloads the first.
         // Interior tiles (not diagonal, no ragged edge) need no masking.
-        const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= a.Lk) && (qb + 1) * kBlk <= a.Lq;
+        const bool interior = (a.causal ? j < qb : (j + 1) * kBlk <= Lk) && (qb + 1) * kBlk <= Lq;
         const int cmax = valid ? lim - j * kBlk : -1;   // last legal column of this row in the tile
         uint32_t sr[64];                        // raw scores Q.K of one half, later packed P
         float mx[8];
@@ -456,7 +462,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.o_done[s]), 0, abortp, a.status) && ok;
       fence_after_sync();
       if (__all_sync(0xffffffffu, ok && !*abortp)) {
-        Tout* orow = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + (valid ? qrow : 0)) * a.Hq + h) * kD;
+        Tout* orow = static_cast<Tout*>(a.o) +
+                     ((static_cast<size_t>(bc) * a.Lq + row0 + (valid ? qrow : 0)) * a.Hq + h) * kD;
         const float inv = 1.f / lr;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -464,8 +471,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           tmem_ld32_sync(lane_addr + colO + c * 32, reinterpret_cast<uint32_t*>(o));
           if (valid) store_row<Tout>(orow + c * 32, o, inv);
         }
-        if (valid) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m_used + log2f(l)) * kLn2;
-        if (a.counts != nullptr && r == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = nret;
+        if (valid) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m_used + log2f(l)) * kLn2;
+        if (a.counts != nullptr && r == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTr + qb] = nret;
       }
       fence_before_sync();
     }
@@ -486,11 +493,12 @@ bool fwd_tc_supported(const FwdArgs& a) {
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, cudaStream_t s, int* launches) {
   CUtensorMap mq, mk, mv;
-  if (!encode_bshd_map(&mq, a.q, a.B, a.Lq, a.Hq, kD, kBlk) ||
-      !encode_bshd_map(&mk, a.k, a.B, a.Lk, a.Hkv, kD, kBlk) ||
-      !encode_bshd_map(&mv, a.v, a.B, a.Lk, a.Hkv, kD, kBlk))
+  const int lb = a.cu ? 1 : a.B;           // a packed batch is one run of Lq rows
+  if (!encode_bshd_map(&mq, a.q, lb, a.Lq, a.Hq, kD, kBlk) ||
+      !encode_bshd_map(&mk, a.k, lb, a.Lk, a.Hkv, kD, kBlk) ||
+      !encode_bshd_map(&mv, a.v, lb, a.Lk, a.Hkv, kD, kBlk))
     return cudaErrorInvalidValue;
-  const int tr = (a.Lq + kBlk - 1) / kBlk;
+  const int tr = ((a.cu ? a.Lmax : a.Lq) + kBlk - 1) / kBlk;
   dim3 grid(a.Hq * a.B, (tr + 1) / 2);
   ++*launches;
   cudaError_t e;

@@ -152,6 +152,87 @@ bool workspace_ok(const void* workspace, size_t workspace_bytes, size_t need) {
   return workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 && workspace_bytes >= need;
 }
 
+// Forward of B sequences of Lq / Lk rows (cu == null) or of a packed batch
+// (cu != null, Lq = Lk = total rows, each sequence at most Lmax long).
+mala_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu,
+                    int batch, int seqlen_q, int seqlen_k, int lmax, int heads_q, int heads_kv, int head_dim,
+                    int in_dtype, int out_dtype, int causal, int block_q, int block_k, float tau,
+                    float softmax_scale, int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  if (!q || !k || !v || !o || !lse) return MALA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return MALA_ERR_INVALID_ARG;
+  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
+                                 out_dtype, causal, block_q, block_k, tau, softmax_scale);
+  if (st != MALA_OK) return st;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.cu = cu; a.Lmax = lmax;
+  a.in_dt = in_dtype; a.out_dt = out_dtype; a.causal = causal; a.blk = block_q;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = fwd_tc_supported(a) ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
+  return finish(e, launches);
+}
+
+// Host-side checks of a packed batch (the bounds themselves are checked on the device).
+bool check_packed(const int32_t* cu, int batch, int total, int lmax) {
+  return cu && (reinterpret_cast<uintptr_t>(cu) & 3u) == 0 && batch >= 1 && total >= 1 && lmax >= 1 &&
+         lmax <= total;
+}
+
+// Backward of B sequences of Lq / Lk rows (cu == null) or of a packed batch
+// (cu != null, Lq = Lk = total rows, each sequence at most Lmax long).
+mala_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                    void* dq, void* dk, void* dv, const int32_t* cu, int batch, int seqlen_q, int seqlen_k,
+                    int lmax, int heads_q, int heads_kv, int head_dim, int in_dtype, int grad_dtype, int causal,
+                    int block_q, int block_k, float tau, float softmax_scale, void* workspace,
+                    size_t workspace_bytes, int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
+  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
+                                 grad_dtype, causal, block_q, block_k, tau, softmax_scale);
+  if (st != MALA_OK) return st;
+  // a packed batch is laid out as one run of seqlen_q = seqlen_k = total rows
+  const BwdLayout w = bwd_layout(cu ? 1 : batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
+                                 grad_dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return MALA_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return MALA_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
+  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.cu = cu; a.Lmax = lmax;
+  a.in_dt = in_dtype; a.grad_dt = grad_dtype; a.causal = causal; a.blk = block_q;
+  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
+  a.scale_log2 = softmax_scale * kLog2e; a.scale = softmax_scale;
+  a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.dq_acc = grad_dtype == MALA_FP32 ? static_cast<float*>(dq) : reinterpret_cast<float*>(ws + w.dq_acc);
+  a.scratch = ws + w.scratch;
+  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  const bool tc = bwd_tc_supported(a);
+  if (!tc && bwd_simt_smem(in_dtype, head_dim, block_q) > 227u * 1024u) return MALA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  if (tc) {
+    e = launch_bwd_tc(a, s, &launches);
+  } else {
+    e = launch_bwd_preprocess(a, s, &launches);
+    if (e == cudaSuccess) e = launch_bwd_simt(a, s, &launches);
+  }
+  if (e == cudaSuccess && grad_dtype == MALA_BF16) e = launch_dq_convert(a, s, &launches);
+  return finish(e, launches);
+}
+
 }  // namespace
 
 extern "C" {
@@ -173,25 +254,21 @@ mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float
                      int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int causal,
                      int block_q, int block_k, float tau, float softmax_scale,
                      int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
-  if (!q || !k || !v || !o || !lse) return MALA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return MALA_ERR_INVALID_ARG;
-  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
-                                 out_dtype, causal, block_q, block_k, tau, softmax_scale);
-  if (st != MALA_OK) return st;
-  int* status = status_word();
-  if (!status) return MALA_ERR_CUDA;
-  FwdArgs a{};
-  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
-  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
-  a.in_dt = in_dtype; a.out_dt = out_dtype; a.causal = causal; a.blk = block_q;
-  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int launches = 0;
-  cudaError_t e = fwd_tc_supported(a) ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
-  return finish(e, launches);
+  return run_fwd(q, k, v, o, lse, nullptr, batch, seqlen_q, seqlen_k, seqlen_q, heads_q, heads_kv, head_dim,
+                 in_dtype, out_dtype, causal, block_q, block_k, tau, softmax_scale, retained_counts, tile_mask,
+                 stream);
+}
+
+mala_status mala_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                            int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                            mala_dtype out_dtype, int causal, int block_q, int block_k, float tau,
+                            float softmax_scale, int32_t* retained_counts, uint8_t* tile_mask,
+                            void* stream) {
+  if (!check_packed(cu_seqlens, batch, total_tokens, max_seqlen)) return MALA_ERR_INVALID_ARG;
+  return run_fwd(q, k, v, o, lse, cu_seqlens, batch, total_tokens, total_tokens, max_seqlen, heads_q, heads_kv,
+                 head_dim, in_dtype, out_dtype, causal, block_q, block_k, tau, softmax_scale, retained_counts,
+                 tile_mask, stream);
 }
 
 size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
@@ -207,41 +284,27 @@ mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
                      int block_q, int block_k, float tau, float softmax_scale,
                      void* workspace, size_t workspace_bytes,
                      int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
-  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return MALA_ERR_INVALID_ARG;
-  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype,
-                                 grad_dtype, causal, block_q, block_k, tau, softmax_scale);
-  if (st != MALA_OK) return st;
-  const BwdLayout w = bwd_layout(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype, grad_dtype);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
-    return MALA_ERR_WORKSPACE;
-  int* status = status_word();
-  if (!status) return MALA_ERR_CUDA;
-  char* ws = static_cast<char*>(workspace);
-  BwdArgs a{};
-  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse; a.dq = dq; a.dk = dk; a.dv = dv;
-  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
-  a.in_dt = in_dtype; a.grad_dt = grad_dtype; a.causal = causal; a.blk = block_q;
-  a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
-  a.scale_log2 = softmax_scale * kLog2e; a.scale = softmax_scale;
-  a.delta = reinterpret_cast<float*>(ws + w.delta);
-  a.dq_acc = grad_dtype == MALA_FP32 ? static_cast<float*>(dq) : reinterpret_cast<float*>(ws + w.dq_acc);
-  a.scratch = ws + w.scratch;
-  a.counts = retained_counts; a.mask = tile_mask; a.status = status;
-  const bool tc = bwd_tc_supported(a);
-  if (!tc && bwd_simt_smem(in_dtype, head_dim, block_q) > 227u * 1024u) return MALA_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int launches = 0;
-  cudaError_t e = cudaSuccess;
-  if (tc) {
-    e = launch_bwd_tc(a, s, &launches);
-  } else {
-    e = launch_bwd_preprocess(a, s, &launches);
-    if (e == cudaSuccess) e = launch_bwd_simt(a, s, &launches);
-  }
-  if (e == cudaSuccess && grad_dtype == MALA_BF16) e = launch_dq_convert(a, s, &launches);
-  return finish(e, launches);
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, nullptr, batch, seqlen_q, seqlen_k, seqlen_q, heads_q,
+                 heads_kv, head_dim, in_dtype, grad_dtype, causal, block_q, block_k, tau, softmax_scale,
+                 workspace, workspace_bytes, retained_counts, tile_mask, stream);
+}
+
+size_t mala_bwd_varlen_workspace_size(int total_tokens, int heads_q, int heads_kv, int head_dim,
+                                      mala_dtype in_dtype, mala_dtype grad_dtype) {
+  return mala_bwd_workspace_size(1, total_tokens, total_tokens, heads_q, heads_kv, head_dim, in_dtype, grad_dtype);
+}
+
+mala_status mala_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            const int32_t* cu_seqlens, int batch, int total_tokens, int max_seqlen,
+                            int heads_q, int heads_kv, int head_dim, mala_dtype in_dtype,
+                            mala_dtype grad_dtype, int causal, int block_q, int block_k, float tau,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  if (!check_packed(cu_seqlens, batch, total_tokens, max_seqlen)) return MALA_ERR_INVALID_ARG;
+  return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, batch, total_tokens, total_tokens, max_seqlen,
+                 heads_q, heads_kv, head_dim, in_dtype, grad_dtype, causal, block_q, block_k, tau, softmax_scale,
+                 workspace, workspace_bytes, retained_counts, tile_mask, stream);
 }
 
 size_t mala_decode_workspace_size(int batch, int heads_q, int head_dim, int num_splits) {

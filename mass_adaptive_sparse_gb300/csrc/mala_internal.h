@@ -17,12 +17,18 @@ enum Dtype : int { kBF16 = 0, kFP32 = 1 };
 // Device status word codes (bitwise OR of events).
 enum StatusCode : int {
   kStatusWaitTimeout = 1,   // an mbarrier wait ran past its time limit
-  kStatusBadLength = 2      // a variable-length decode sequence length was outside [1, N]
+  kStatusBadLength = 2      // a variable-length sequence (decode cache length or packed prefill bounds) was invalid
 };
 
+// Prefill calls take either B sequences of Lq query / Lk key rows ([B, L, H, D]
+// tensors, cu == null), or B sequences of different lengths packed along one
+// token axis of Lq = Lk = total rows ([total, H, D] tensors, lse [Hq, total]),
+// sequence b holding rows cu[b] .. cu[b + 1] - 1 and none longer than Lmax.
 struct FwdArgs {
   const void* q; const void* k; const void* v; void* o; float* lse;
   int B, Lq, Lk, Hq, Hkv, D;
+  const int32_t* cu;    // [B + 1] sequence starts (device) of a packed batch, or null
+  int Lmax;             // longest sequence: tile rows of mask / counts and the grid
   int in_dt, out_dt, causal, blk;
   float tau;            // >= 0; 0 = dense
   float log2_tau;       // log2(tau), used only when tau > 0
@@ -36,6 +42,8 @@ struct BwdArgs {
   const void* q; const void* k; const void* v; const void* o; const void* dout;
   const float* lse; void* dq; void* dk; void* dv;
   int B, Lq, Lk, Hq, Hkv, D;
+  const int32_t* cu;    // as FwdArgs
+  int Lmax;
   int in_dt, grad_dt, causal, blk;
   float tau, log2_tau, scale_log2, scale;
   float* delta;         // workspace: D_i = rowsum(O * dO)   [B, Hq, Lq]
@@ -61,6 +69,25 @@ struct DecArgs {
 };
 
 #ifdef __CUDACC__
+// Sequence b of a prefill call: its query / key lengths, the row of its first
+// token and its batch coordinate in the tensors' layout (0 for a packed batch).
+// A packed sequence whose bounds are not 0 <= cu[b] <= cu[b + 1] <= total with
+// at most Lmax rows raises kStatusBadLength and comes back empty.
+struct SeqSpan {
+  int Lq, Lk, row0, bc;
+};
+
+template <typename Args>
+__device__ __forceinline__ SeqSpan seq_span(const Args& a, int b) {
+  if (a.cu == nullptr) return {a.Lq, a.Lk, 0, b};
+  const int s0 = a.cu[b], s1 = a.cu[b + 1];
+  if (s0 < 0 || s1 < s0 || s1 > a.Lq || s1 - s0 > a.Lmax) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadLength);
+    return {0, 0, 0, 0};
+  }
+  return {s1 - s0, s1 - s0, s0, 0};
+}
+
 // Cache length of sequence b: N, or lens[b] for a variable-length decode.  A
 // length outside [1, N] raises kStatusBadLength and gives 0 (no keys: the
 // sequence's output and lse come out NaN).

@@ -58,17 +58,25 @@ fwd_simt_kernel(const FwdArgs a) {
   float* Ss = Vs + BLK * D;                   // [BLK][SS] scores, log2 units
 
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // this CTA's sequence: its lengths, first row and batch coordinate in the layout
+  const SeqSpan sq = seq_span(a, b);
+  const int Lq = sq.Lq, Lk = sq.Lk, row0 = sq.row0, bc = sq.bc;
+  const int Tr = (Lq + BLK - 1) / BLK;
+  const int Tc = (Lk + BLK - 1) / BLK;
+  if (qb >= Tr) return;                   // past the sequence's query blocks (packed batches)
+  // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
+  const int mTr = a.cu ? (a.Lmax + BLK - 1) / BLK : Tr, mTc = a.cu ? mTr : Tc;
   const int hk = h / (a.Hq / a.Hkv);
   const int tid = threadIdx.x, r = tid / TPR, part = tid % TPR;
   const int qrow = qb * BLK + r;
-  const bool row_valid = qrow < a.Lq;
+  const bool row_valid = qrow < Lq;
   const Tin* qg = static_cast<const Tin*>(a.q);
   const Tin* kg = static_cast<const Tin*>(a.k);
   const Tin* vg = static_cast<const Tin*>(a.v);
 
   float qv[32], acc[32];
   {
-    const Tin* qp = qg + ((static_cast<size_t>(b) * a.Lq + (row_valid ? qrow : 0)) * a.Hq + h) * D;
+    const Tin* qp = qg + ((static_cast<size_t>(bc) * a.Lq + row0 + (row_valid ? qrow : 0)) * a.Hq + h) * D;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       qv[c] = row_valid ? ld(qp + c * TPR + part) * a.scale_log2 : 0.f;
@@ -76,12 +84,10 @@ fwd_simt_kernel(const FwdArgs a) {
     }
   }
   float m = -INFINITY, l = 0.f;
-  const float lvis = a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(a.Lk);
+  const float lvis = a.causal ? static_cast<float>(qrow + 1) : static_cast<float>(Lk);
   const float thr = a.log2_tau - log2f(lvis);
   const bool test = a.tau > 0.f;
-  const int Tr = (a.Lq + BLK - 1) / BLK;
-  const int Tc = (a.Lk + BLK - 1) / BLK;
-  const int jtop = a.causal ? min(Tc - 1, (min(a.Lq, qb * BLK + BLK) - 1) / BLK) : Tc - 1;
+  const int jtop = a.causal ? min(Tc - 1, (min(Lq, qb * BLK + BLK) - 1) / BLK) : Tc - 1;
   int kept = 0;
 
   for (int j = jtop; j >= 0; --j) {
@@ -89,7 +95,7 @@ fwd_simt_kernel(const FwdArgs a) {
     __syncthreads();
     for (int idx = tid; idx < BLK * D; idx += NT) {
       const int kr = idx / D, c = idx % D, key = k0 + kr;
-      Ks[idx] = key < a.Lk ? ld(kg + ((static_cast<size_t>(b) * a.Lk + key) * a.Hkv + hk) * D + c) : 0.f;
+      Ks[idx] = key < Lk ? ld(kg + ((static_cast<size_t>(bc) * a.Lk + row0 + key) * a.Hkv + hk) * D + c) : 0.f;
     }
     __syncthreads();
     float mt = -INFINITY;
@@ -99,7 +105,7 @@ fwd_simt_kernel(const FwdArgs a) {
       for (int c = 0; c < 32; ++c) s = fmaf(qv[c], Ks[kr * D + c * TPR + part], s);
       s = row_sum<TPR>(s);
       const int key = k0 + kr;
-      const bool legal = row_valid && key < a.Lk && (!a.causal || key <= qrow);
+      const bool legal = row_valid && key < Lk && (!a.causal || key <= qrow);
       s = legal ? s : -INFINITY;
       mt = fmaxf(mt, s);
       if (part == 0) Ss[r * SS + kr] = s;
@@ -111,12 +117,12 @@ fwd_simt_kernel(const FwdArgs a) {
       keep_row = !test || l == 0.f || !(mt - m - log2f(l) < thr);
     const int keep = __syncthreads_or(keep_row);
     if (a.mask != nullptr && tid == 0)
-      a.mask[((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc + j] = keep ? 1 : 0;
+      a.mask[((static_cast<size_t>(b) * a.Hq + h) * mTr + qb) * mTc + j] = keep ? 1 : 0;
     if (!keep) continue;
     ++kept;
     for (int idx = tid; idx < BLK * D; idx += NT) {
       const int kr = idx / D, c = idx % D, key = k0 + kr;
-      Vs[idx] = key < a.Lk ? ld(vg + ((static_cast<size_t>(b) * a.Lk + key) * a.Hkv + hk) * D + c) : 0.f;
+      Vs[idx] = key < Lk ? ld(vg + ((static_cast<size_t>(bc) * a.Lk + row0 + key) * a.Hkv + hk) * D + c) : 0.f;
     }
     __syncthreads();
     if (mt > -INFINITY) {
@@ -135,13 +141,13 @@ fwd_simt_kernel(const FwdArgs a) {
     }
   }
   if (row_valid) {
-    Tout* op = static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.Lq + qrow) * a.Hq + h) * D;
+    Tout* op = static_cast<Tout*>(a.o) + ((static_cast<size_t>(bc) * a.Lq + row0 + qrow) * a.Hq + h) * D;
     const float inv = 1.f / l;
 #pragma unroll
     for (int c = 0; c < 32; ++c) st(op + c * TPR + part, acc[c] * inv);
-    if (part == 0) a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qrow] = (m + log2f(l)) * kLn2;
+    if (part == 0) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m + log2f(l)) * kLn2;
   }
-  if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tr + qb] = kept;
+  if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTr + qb] = kept;
 }
 
 // ---------------------------------------------------------------------------
@@ -150,7 +156,7 @@ fwd_simt_kernel(const FwdArgs a) {
 // ---------------------------------------------------------------------------
 template <typename Tin>
 __global__ void bwd_preprocess_kernel(const BwdArgs a) {
-  const size_t rows = static_cast<size_t>(a.B) * a.Lq * a.Hq;
+  const size_t rows = static_cast<size_t>(a.cu ? 1 : a.B) * a.Lq * a.Hq;   // a packed batch: one run
   const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -175,7 +181,7 @@ __global__ void bwd_preprocess_kernel(const BwdArgs a) {
 
 template <typename Tg>
 __global__ void dq_convert_kernel(const BwdArgs a) {
-  const size_t n = static_cast<size_t>(a.B) * a.Lq * a.Hq * a.D;
+  const size_t n = static_cast<size_t>(a.cu ? 1 : a.B) * a.Lq * a.Hq * a.D;
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
     st(static_cast<Tg*>(a.dq) + i, a.dq_acc[i]);
@@ -205,6 +211,14 @@ bwd_simt_kernel(const BwdArgs a) {
   float* thr = dlt + BLK;                      // [BLK]
 
   const int kb = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  // this CTA's sequence: its lengths, first row and batch coordinate in the layout
+  const SeqSpan sq = seq_span(a, b);
+  const int Lq = sq.Lq, Lk = sq.Lk, row0 = sq.row0, bc = sq.bc;
+  const int Tr = (Lq + BLK - 1) / BLK;
+  const int Tc = (Lk + BLK - 1) / BLK;
+  if (kb >= Tc) return;                   // past the sequence's key blocks (packed batches)
+  // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
+  const int mTr = a.cu ? (a.Lmax + BLK - 1) / BLK : Tr, mTc = a.cu ? mTr : Tc;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, kr = tid / TPR, part = tid % TPR;
   const int key = kb * BLK + kr;
@@ -212,15 +226,13 @@ bwd_simt_kernel(const BwdArgs a) {
   const Tin* kg = static_cast<const Tin*>(a.k);
   const Tin* vg = static_cast<const Tin*>(a.v);
   const Tin* dog = static_cast<const Tin*>(a.dout);
-  const int Tr = (a.Lq + BLK - 1) / BLK;
-  const int Tc = (a.Lk + BLK - 1) / BLK;
   const bool test = a.tau > 0.f;
 
   for (int idx = tid; idx < BLK * D; idx += NT) {
     const int rr = idx / D, c = idx % D, kk = kb * BLK + rr;
-    const size_t off = ((static_cast<size_t>(b) * a.Lk + kk) * a.Hkv + hk) * D + c;
-    Ks[rr * KS + c] = kk < a.Lk ? kg[off] : zero<Tin>();
-    Vs[rr * KS + c] = kk < a.Lk ? vg[off] : zero<Tin>();
+    const size_t off = ((static_cast<size_t>(bc) * a.Lk + row0 + (kk < Lk ? kk : 0)) * a.Hkv + hk) * D + c;
+    Ks[rr * KS + c] = kk < Lk ? kg[off] : zero<Tin>();
+    Vs[rr * KS + c] = kk < Lk ? vg[off] : zero<Tin>();
   }
   float dk[32], dv[32];
 #pragma unroll
@@ -235,16 +247,16 @@ bwd_simt_kernel(const BwdArgs a) {
       __syncthreads();
       for (int idx = tid; idx < BLK * D; idx += NT) {
         const int rr = idx / D, c = idx % D, qq = q0 + rr;
-        const size_t off = ((static_cast<size_t>(b) * a.Lq + qq) * a.Hq + h) * D + c;
-        Qs[idx] = qq < a.Lq ? qg[off] : zero<Tin>();
-        dOs[idx] = qq < a.Lq ? dog[off] : zero<Tin>();
+        const size_t off = ((static_cast<size_t>(bc) * a.Lq + row0 + (qq < Lq ? qq : 0)) * a.Hq + h) * D + c;
+        Qs[idx] = qq < Lq ? qg[off] : zero<Tin>();
+        dOs[idx] = qq < Lq ? dog[off] : zero<Tin>();
       }
       for (int rr = tid; rr < BLK; rr += NT) {
         const int qq = q0 + rr;
-        const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.Lq + qq;
-        lse2[rr] = qq < a.Lq ? a.lse[off] * kLog2e : 0.f;
-        dlt[rr] = qq < a.Lq ? a.delta[off] : 0.f;
-        thr[rr] = a.log2_tau - log2f(a.causal ? static_cast<float>(qq + 1) : static_cast<float>(a.Lk));
+        const size_t off = (static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + (qq < Lq ? qq : 0);
+        lse2[rr] = qq < Lq ? a.lse[off] * kLog2e : 0.f;
+        dlt[rr] = qq < Lq ? a.delta[off] : 0.f;
+        thr[rr] = a.log2_tau - log2f(a.causal ? static_cast<float>(qq + 1) : static_cast<float>(Lk));
       }
       __syncthreads();
       // Scores S^T of this tile; Eq. (4): keep iff some valid entry has
@@ -257,14 +269,14 @@ bwd_simt_kernel(const BwdArgs a) {
           s = fmaf(ld(Ks + kr * KS + c * TPR + part), ld(Qs + qq * D + c * TPR + part), s);
         s = row_sum<TPR>(s) * a.scale_log2;
         const int qrow = q0 + qq;
-        const bool valid = key < a.Lk && qrow < a.Lq && (!a.causal || key <= qrow);
+        const bool valid = key < Lk && qrow < Lq && (!a.causal || key <= qrow);
         s = valid ? s : -INFINITY;
         if (valid && (!test || !(s - lse2[qq] < thr[qq]))) keep_local = true;
         if (part == 0) Ss[kr * SS + qq] = s;
       }
       const int keep = __syncthreads_or(keep_local);
       if (a.mask != nullptr && tid == 0)
-        a.mask[((static_cast<size_t>(b) * a.Hq + h) * Tr + i) * Tc + kb] = keep ? 1 : 0;
+        a.mask[((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb] = keep ? 1 : 0;
       if (!keep) continue;
       ++kept;
       for (int qq = 0; qq < BLK; ++qq) {
@@ -288,8 +300,8 @@ bwd_simt_kernel(const BwdArgs a) {
       {
         const int qq = tid / TPR;
         const int qrow = q0 + qq;
-        if (qrow < a.Lq) {
-          float* dqp = a.dq_acc + ((static_cast<size_t>(b) * a.Lq + qrow) * a.Hq + h) * D;
+        if (qrow < Lq) {
+          float* dqp = a.dq_acc + ((static_cast<size_t>(bc) * a.Lq + row0 + qrow) * a.Hq + h) * D;
           for (int c = 0; c < 32; ++c) {
             float sum = 0.f;
             for (int k2 = 0; k2 < BLK; ++k2)
@@ -299,10 +311,10 @@ bwd_simt_kernel(const BwdArgs a) {
         }
       }
     }
-    if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * Tc + kb] = kept;
+    if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTc + kb] = kept;
   }
-  if (key < a.Lk) {
-    const size_t off = ((static_cast<size_t>(b) * a.Lk + key) * a.Hkv + hk) * D;
+  if (key < Lk) {
+    const size_t off = ((static_cast<size_t>(bc) * a.Lk + row0 + key) * a.Hkv + hk) * D;
     Tg* dkp = static_cast<Tg*>(a.dk) + off;
     Tg* dvp = static_cast<Tg*>(a.dv) + off;
 #pragma unroll
@@ -519,7 +531,7 @@ cudaError_t fwd_go(const FwdArgs& a, cudaStream_t s) {
   auto kern = fwd_simt_kernel<Tin, Tout, D, BLK>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Lq + BLK - 1) / BLK, a.Hq, a.B);
+  dim3 grid(((a.cu ? a.Lmax : a.Lq) + BLK - 1) / BLK, a.Hq, a.B);
   kern<<<grid, BLK * (D / 32), smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -538,7 +550,7 @@ cudaError_t bwd_go(const BwdArgs& a, cudaStream_t s) {
   auto kern = bwd_simt_kernel<Tin, Tg, D, BLK>;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Lk + BLK - 1) / BLK, a.Hkv, a.B);
+  dim3 grid(((a.cu ? a.Lmax : a.Lk) + BLK - 1) / BLK, a.Hkv, a.B);
   kern<<<grid, BLK * (D / 32), smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -601,7 +613,7 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s, int* launches) {
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s, int* launches) {
   ++*launches;
-  const size_t rows = static_cast<size_t>(a.B) * a.Lq * a.Hq;
+  const size_t rows = static_cast<size_t>(a.cu ? 1 : a.B) * a.Lq * a.Hq;   // a packed batch: one run
   const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
   if (a.in_dt == kBF16) bwd_preprocess_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(a);
   else bwd_preprocess_kernel<float><<<blocks, 256, 0, s>>>(a);
@@ -617,7 +629,7 @@ cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s, int* launches) {
 
 cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s, int* launches) {
   ++*launches;
-  const size_t n = static_cast<size_t>(a.B) * a.Lq * a.Hq * a.D;
+  const size_t n = static_cast<size_t>(a.cu ? 1 : a.B) * a.Lq * a.Hq * a.D;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 152u * 16u));
   if (a.grad_dt == kBF16) dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(a);
   else dq_convert_kernel<float><<<blocks, 256, 0, s>>>(a);

@@ -44,7 +44,8 @@ __all__ = [
     "visible_key_counts", "dense_attention", "dense_attention_grads",
     "restricted_attention", "mala_forward", "mala_backward",
     "block_summary", "merge_summaries", "mala_decode",
-    "mala_forward_bshd", "mala_backward_bshd", "mala_decode_bhd", "mala_decode_per_head_bhd",
+    "mala_forward_bshd", "mala_backward_bshd", "mala_forward_varlen", "mala_backward_varlen",
+    "mala_decode_bhd", "mala_decode_per_head_bhd",
     "mala_decode_varlen_bhd",
     "omitted_mass", "BORDERLINE_REL",
 ]
@@ -442,6 +443,65 @@ def mala_backward_bshd(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, hea
             out["retained"][b, h] = r.retained
             out["legal"][b, h] = r.legal
             out["margin"][b, h] = r.margin
+    return out
+
+
+def mala_forward_varlen(q, k, v, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None):
+    """Packed variable-length forward: sequence b is rows cu_seqlens[b] ..
+    cu_seqlens[b + 1] - 1 of q [total, Hq, d], k / v [total, Hkv, d] and is
+    its own context (§2.1 counts L_q per row within it), i.e. exactly
+    ``mala_forward_bshd`` on that slice.  Returns o [total, Hq, d], lse
+    [Hq, total] and retained / legal / margin [B, Hq, Tm, Tm] with
+    Tm = ceil(max length / bq) (entries past a sequence's tiles False / NaN)."""
+    total, hq, d = q.shape
+    nseq = len(cu_seqlens) - 1
+    lens = [int(cu_seqlens[b + 1]) - int(cu_seqlens[b]) for b in range(nseq)]
+    tm = -(-max(lens) // bq)
+    out = {
+        "o": np.zeros((total, hq, v.shape[2])),
+        "lse": np.full((hq, total), np.nan),
+        "retained": np.zeros((nseq, hq, tm, tm), dtype=bool),
+        "legal": np.zeros((nseq, hq, tm, tm), dtype=bool),
+        "margin": np.full((nseq, hq, tm, tm), np.nan),
+    }
+    for b in (range(nseq) if seqs is None else seqs):
+        s0, n = int(cu_seqlens[b]), lens[b]
+        if n == 0:
+            continue
+        r = mala_forward_bshd(q[None, s0:s0 + n], k[None, s0:s0 + n], v[None, s0:s0 + n], scale, tau, bq, bk,
+                              causal, heads=heads)
+        t = -(-n // bq)
+        out["o"][s0:s0 + n] = r["o"][0]
+        out["lse"][:, s0:s0 + n] = r["lse"][0]
+        for key in ("retained", "legal", "margin"):
+            out[key][b, :, :t, :t] = r[key][0]
+    return out
+
+
+def mala_backward_varlen(q, k, v, o, do, lse, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None):
+    """Packed variable-length backward (layouts as ``mala_forward_varlen``):
+    ``mala_backward_bshd`` on each sequence's slice."""
+    total, hq, d = q.shape
+    nseq = len(cu_seqlens) - 1
+    lens = [int(cu_seqlens[b + 1]) - int(cu_seqlens[b]) for b in range(nseq)]
+    tm = -(-max(lens) // bq)
+    out = {"dq": np.zeros(q.shape), "dk": np.zeros(k.shape), "dv": np.zeros(v.shape),
+           "retained": np.zeros((nseq, hq, tm, tm), dtype=bool),
+           "legal": np.zeros((nseq, hq, tm, tm), dtype=bool),
+           "margin": np.full((nseq, hq, tm, tm), np.nan)}
+    for b in (range(nseq) if seqs is None else seqs):
+        s0, n = int(cu_seqlens[b]), lens[b]
+        if n == 0:
+            continue
+        sl = slice(s0, s0 + n)
+        r = mala_backward_bshd(q[None, sl], k[None, sl], v[None, sl], o[None, sl], do[None, sl],
+                               lse[None, :, sl], scale, tau, bq, bk, causal, heads=heads)
+        t = -(-n // bq)
+        out["dq"][sl] = r["dq"][0]
+        out["dk"][sl] = r["dk"][0]
+        out["dv"][sl] = r["dv"][0]
+        for key in ("retained", "legal", "margin"):
+            out[key][b, :, :t, :t] = r[key][0]
     return out
 
 

@@ -515,3 +515,44 @@ def test_decode_per_head_with_single_head_groups_is_the_group_decode():
     b = orc.mala_decode_bhd(q, k, v, 0.25, 2.0, 32, 3)
     np.testing.assert_array_equal(a["retained"], b["retained"])
     np.testing.assert_allclose(a["o"], b["o"], rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length prefill: each sequence is its own context.
+# ---------------------------------------------------------------------------
+
+def test_varlen_tau0_is_dense_causal_per_sequence():
+    lens = [1, 5, 40, 17]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v = _rand((63, 2, 8), 131, 2.0), _rand((63, 1, 8), 132), _rand((63, 1, 8), 133)
+    r = orc.mala_forward_varlen(q, k, v, cu, 0.3, 0.0, 8, 8)
+    for b, n in enumerate(lens):
+        sl = slice(cu[b], cu[b + 1])
+        for h in range(2):
+            o_ref, lse_ref = _sdpa(q[sl, h], k[sl, 0], v[sl, 0], 0.3, causal=True)
+            np.testing.assert_allclose(r["o"][sl, h], o_ref, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(r["lse"][h, sl], lse_ref, rtol=1e-12, atol=1e-12)
+    do = _rand((63, 2, 8), 134)
+    g = orc.mala_backward_varlen(q, k, v, r["o"], do, r["lse"], cu, 0.3, 0.0, 8, 8)
+    for b, n in enumerate(lens):
+        sl = slice(cu[b], cu[b + 1])
+        dk_sum = np.zeros((n, 8))
+        dv_sum = np.zeros((n, 8))
+        for h in range(2):
+            dq_r, dk_r, dv_r = _sdpa_grads(q[sl, h], k[sl, 0], v[sl, 0], do[sl, h], 0.3)
+            np.testing.assert_allclose(g["dq"][sl, h], dq_r, rtol=1e-10, atol=1e-12)
+            dk_sum += dk_r
+            dv_sum += dv_r
+        np.testing.assert_allclose(g["dk"][sl, 0], dk_sum, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dv"][sl, 0], dv_sum, rtol=1e-10, atol=1e-12)
+
+
+def test_varlen_equal_lengths_is_the_batched_layout():
+    """Packing B sequences of L rows is the [B, L, H, d] batch laid end to end."""
+    q, k, v = _rand((3, 40, 2, 8), 141, 2.0), _rand((3, 40, 2, 8), 142), _rand((3, 40, 2, 8), 143)
+    a = orc.mala_forward_varlen(q.reshape(120, 2, 8), k.reshape(120, 2, 8), v.reshape(120, 2, 8),
+                                [0, 40, 80, 120], 0.35, 2.0, 8, 8)
+    b = orc.mala_forward_bshd(q, k, v, 0.35, 2.0, 8, 8)
+    np.testing.assert_array_equal(a["o"], b["o"].reshape(120, 2, 8))
+    np.testing.assert_array_equal(a["lse"], b["lse"].transpose(1, 0, 2).reshape(2, 120))
+    np.testing.assert_array_equal(a["retained"], b["retained"])
