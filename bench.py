@@ -396,45 +396,96 @@ def main():
         t_dense = timed(0.0, args.steps)
 
     # --- end to end through the public API with host buffers ---
+    # The prefill runs in head chunks (heads are independent), so that one
+    # chunk's inputs arrive while the other computes and one chunk's gradients
+    # leave while the other's backward runs.  Four streams: copies in (in the
+    # order they are needed), compute, the decode (as soon as its cache is in,
+    # alongside the prefill), copies out.
     e2e = None
     if not args.no_e2e:
-        host_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True)
-                    for n in ("o", "lse", "dq", "dk", "dv", "od", "lsed")}
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        nchunk = 2 if pc.Hkv % 2 == 0 else 1
+        hk_per = pc.Hkv // nchunk
+        hq_per = hk_per * (pc.H // pc.Hkv)
+        chunks = []
+        for c in range(nchunk):
+            hq = slice(c * hq_per, (c + 1) * hq_per)
+            hkv = slice(c * hk_per, (c + 1) * hk_per)
+            hin = {n: host_in[n][:, :, hq if n in ("q", "do") else hkv].contiguous().pin_memory()
+                   for n in ("q", "k", "v", "do")}
+            dev_c = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in hin.items()}
+            dev_c["o"] = torch.empty_like(dev_c["q"])
+            dev_c["lse"] = torch.empty((B, hq_per, L), dtype=torch.float32, device=dev)
+            for n, like in (("dq", "q"), ("dk", "k"), ("dv", "v")):
+                dev_c[n] = torch.empty(dev_c[like].shape, dtype=torch.float32, device=dev)
+            dev_c["ws"] = torch.empty(max(256, api.mala_bwd_workspace_size(dev_c["q"], dev_c["k"], torch.float32)),
+                                      dtype=torch.uint8, device=dev)
+            hout = {n: torch.empty(dev_c[n].shape, dtype=dev_c[n].dtype, pin_memory=True)
+                    for n in ("o", "lse", "dq", "dk", "dv")}
+            chunks.append((hin, dev_c, hout))
+        dec_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True) for n in ("od", "lsed")}
+        h2d = sum(t.numel() * t.element_size() for c in chunks for t in c[0].values()) + \
+            sum(host_in[n].numel() * host_in[n].element_size() for n in ("qd", "kc", "vc"))
+        d2h = sum(t.numel() * t.element_size() for c in chunks for t in c[2].values()) + \
+            sum(t.numel() * t.element_size() for t in dec_out.values())
 
-        # the prefill and the decode on their own streams, O / lse read back
-        # on a third while the backward runs; each step joins all three
-        sp, sd, so = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        def fwd_c(x):
+            api.mala_fwd(x["q"], x["k"], x["v"], x["o"], x["lse"], block=pc.block, tau=tau)
+
+        def bwd_c(x):
+            api.mala_bwd(x["q"], x["k"], x["v"], x["o"], x["do"], x["lse"], x["dq"], x["dk"], x["dv"], x["ws"],
+                         block=pc.block, tau=tau)
+
+        s_in, s_cmp, s_dec, s_out = (torch.cuda.Stream(dev) for _ in range(4))
+
+        def ev(st_):
+            e_ = torch.cuda.Event()
+            e_.record(st_)
+            return e_
 
         def e2e_step():
-            start = torch.cuda.Event()
-            start.record(stream)
-            for st_ in (sp, sd, so):
+            start = ev(stream)
+            for st_ in (s_in, s_cmp, s_dec, s_out):
                 st_.wait_event(start)
-            with torch.cuda.stream(sp):
-                for n in ("q", "k", "v", "do"):
-                    d[n].copy_(host_in[n], non_blocking=True)
-                fwd(tau)
-                fwd_done = torch.cuda.Event()
-                fwd_done.record(sp)
-                bwd(tau)
-                for n in ("dq", "dk", "dv"):
-                    host_out[n].copy_(d[n], non_blocking=True)
-            with torch.cuda.stream(sd):
+            with torch.cuda.stream(s_in):
+                in_qkv, in_do = [], []
+                for hin, dev_c, _ in chunks:
+                    for n in ("q", "k", "v"):
+                        dev_c[n].copy_(hin[n], non_blocking=True)
+                    in_qkv.append(ev(s_in))
+                for hin, dev_c, _ in chunks:
+                    dev_c["do"].copy_(hin["do"], non_blocking=True)
+                    in_do.append(ev(s_in))
                 for n in ("qd", "kc", "vc"):
                     d[n].copy_(host_in[n], non_blocking=True)
+                in_cache = ev(s_in)
+            with torch.cuda.stream(s_cmp):
+                done_f, done_b = [], []
+                for i, (_, dev_c, _) in enumerate(chunks):
+                    s_cmp.wait_event(in_qkv[i])
+                    fwd_c(dev_c)
+                    done_f.append(ev(s_cmp))
+                for i, (_, dev_c, _) in enumerate(chunks):
+                    s_cmp.wait_event(in_do[i])
+                    bwd_c(dev_c)
+                    done_b.append(ev(s_cmp))
+            with torch.cuda.stream(s_dec):
+                s_dec.wait_event(in_cache)
                 dec(tau)
+                done_d = ev(s_dec)
+            with torch.cuda.stream(s_out):
+                for i, (_, dev_c, hout) in enumerate(chunks):
+                    s_out.wait_event(done_f[i])
+                    for n in ("o", "lse"):
+                        hout[n].copy_(dev_c[n], non_blocking=True)
+                for i, (_, dev_c, hout) in enumerate(chunks):
+                    s_out.wait_event(done_b[i])
+                    for n in ("dq", "dk", "dv"):
+                        hout[n].copy_(dev_c[n], non_blocking=True)
+                s_out.wait_event(done_d)
                 for n in ("od", "lsed"):
-                    host_out[n].copy_(d[n], non_blocking=True)
-            so.wait_event(fwd_done)
-            with torch.cuda.stream(so):
-                for n in ("o", "lse"):
-                    host_out[n].copy_(d[n], non_blocking=True)
-            for st_ in (sp, sd, so):
-                done = torch.cuda.Event()
-                done.record(st_)
-                stream.wait_event(done)
+                    dec_out[n].copy_(d[n], non_blocking=True)
+            for st_ in (s_in, s_cmp, s_dec, s_out):
+                stream.wait_event(ev(st_))
 
         e2e_step()
         barrier()
@@ -447,7 +498,10 @@ def main():
         barrier()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e, "streams": "prefill, decode and O/lse read-back on three streams"}
+               "steps": n_e2e,
+               "pipeline": f"prefill in {nchunk} head chunks; copies in, compute, decode and copies out on "
+                           "four streams"}
+        del chunks
 
     if rank != 0:
         if dist is not None:
