@@ -317,13 +317,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       for (int t = first; ok && t < ntiles; ++t) {
         const int vs = t % kNV, u = t - first;
         const bool more = t + 1 < ntiles;
-        // everything this turn needs, gathered before taking it
+        // everything this turn needs, gathered before taking it, in the order
+        // it becomes ready (P last but the turn)
         ok = mbar_wait(smem_u32(&bars.dec[s][u & 1]), (u >> 1) & 1, abortp, a.status);
         const bool keep = ok && keep_flag[s][u & 1];
-        if (keep)
-          ok = mbar_wait(smem_u32(&bars.p_ready[s]), nkeep & 1, abortp, a.status) &&
-               mbar_wait(smem_u32(&bars.v_full[vs]), (t / kNV) & 1, abortp, a.status);
         if (ok && more) ok = wait_k(t + 1);
+        if (keep) ok = ok && mbar_wait(smem_u32(&bars.v_full[vs]), (t / kNV) & 1, abortp, a.status);
+        if (keep) ok = ok && mbar_wait(smem_u32(&bars.p_ready[s]), nkeep & 1, abortp, a.status);
         ok = ok && take_turn();
         if (!ok) break;
         fence_after_sync();
