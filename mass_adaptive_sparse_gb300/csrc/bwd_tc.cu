@@ -61,7 +61,7 @@ struct Bars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full, do_empty;
-  uint64_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free;
+  uint64_t s_full, dec, p_ready, dp_full, ds_ready, dq_full, dq_free;
   uint64_t fin;
 };
 
@@ -149,6 +149,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     mbar_init(smem_u32(&bars.do_full), 1);
     mbar_init(smem_u32(&bars.do_empty), 1);
     mbar_init(smem_u32(&bars.s_full), 1);
+    mbar_init(smem_u32(&bars.dec), 1);
     mbar_init(smem_u32(&bars.p_ready), 1);
     mbar_init(smem_u32(&bars.dp_full), 1);
     mbar_init(smem_u32(&bars.ds_ready), 1);
@@ -215,13 +216,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       int nret = 0;
       int pend = -1, pend_region = 0;       // retained tile whose dQ^T awaits read-out, and its region
       for (int t = 0; ok && t < ntiles; ++t) {
-        if (!mbar_wait(smem_u32(&bars.p_ready), t & 1, abortp, a.status)) break;
-        fence_after_sync();
+        // the tile's decision comes at the vote; a kept tile's dO (requested
+        // then) is waited for while P is formed, and P, the last to be ready, last
+        if (!mbar_wait(smem_u32(&bars.dec), t & 1, abortp, a.status)) break;
         const int ret = flag;
         const uint32_t qb = sQ + (t & 1) * kTile;
         const uint32_t rg = tmem + region(t);
         if (ret) {
-          if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status)) break;
+          if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status) ||
+              !mbar_wait(smem_u32(&bars.p_ready), nret & 1, abortp, a.status))
+            break;
           fence_after_sync();
           // dV += P^T dO   (A = P^T from TMEM: queries 0-63 packed in the region's
           // columns 0-31, queries 64-127 in columns 64-95, each written by its math group)
@@ -410,7 +414,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (tid == 0) {
           if (mrow) *mrow = 0;
           flag = 0;
-          mbar_arrive(smem_u32(&bars.p_ready));
+          mbar_arrive(smem_u32(&bars.dec));
         }
         // the previous retained tile's dQ is read out here too: the MMA warp
         // waits for it before the scores of tile t + 1 go into its region
@@ -422,6 +426,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       if (tid == 0) {
         if (mrow) *mrow = 1;
+        flag = 1;
+        mbar_arrive(smem_u32(&bars.dec));
         // dO of this tile, loaded only now that the tile is retained
         if (nret > 0) ok = mbar_wait(smem_u32(&bars.do_empty), (nret - 1) & 1, abortp, a.status);
         if (ok) {
@@ -466,10 +472,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       tmem_st_wait();
       fence_before_sync();
       if (named_vote_or(1, kMath, !ok || *abortp)) break;
-      if (tid == 0) {
-        flag = 1;
-        mbar_arrive(smem_u32(&bars.p_ready));
-      }
+      if (tid == 0) mbar_arrive(smem_u32(&bars.p_ready));
       // the previous retained tile's dQ is read out while dV and dP^T run; the
       // MMA warp waits for it only before the next scores go into its region
       if (nret > flushed) {
