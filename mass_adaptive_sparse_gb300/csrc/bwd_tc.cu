@@ -60,7 +60,7 @@ __device__ __forceinline__ uint32_t region(int t) { return static_cast<uint32_t>
 struct Bars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
-  uint64_t do_full, do_empty;
+  uint64_t do_full;
   uint64_t s_full, dec, p_ready, dp_full, ds_ready, dq_full, dq_free;
   uint64_t fin;
 };
@@ -147,7 +147,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     mbar_init(smem_u32(&bars.kv_full), 1);
     for (int i = 0; i < 2; ++i) { mbar_init(smem_u32(&bars.q_full[i]), 1); mbar_init(smem_u32(&bars.q_empty[i]), 1); }
     mbar_init(smem_u32(&bars.do_full), 1);
-    mbar_init(smem_u32(&bars.do_empty), 1);
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.dec), 1);
     mbar_init(smem_u32(&bars.p_ready), 1);
@@ -188,9 +187,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row0 + i * kBlk, bc);
         ++issued;
       }
-      mbar_wait(kvf, 0, abortp, a.status);
+      // every issued load lands before the CTA can finish, abort or not
+      mbar_drain(kvf, 0, a.status);
       for (int t = max(0, issued - 2); t < issued; ++t)
-        mbar_wait(smem_u32(&bars.q_full[t & 1]), (t >> 1) & 1, abortp, a.status);
+        mbar_drain(smem_u32(&bars.q_full[t & 1]), (t >> 1) & 1, a.status);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
@@ -240,7 +240,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mma_ss(rg, desc_kmajor_sw128(sV + off), desc_kmajor_sw128(sDO + off), id_kk, k > 0);
           }
           mma_commit(smem_u32(&bars.dp_full));
-          mma_commit(smem_u32(&bars.do_empty));
         }
         // the next scores into the other region, once the dQ^T left there has been read out
         if (t + 1 < ntiles) {
@@ -275,7 +274,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         ++nret;
       }
       mma_commit(smem_u32(&bars.fin));
-      mbar_wait(smem_u32(&bars.fin), 0, abortp, a.status);
+      mbar_drain(smem_u32(&bars.fin), 0, a.status);
     }
   } else {
     // ---------------- math warpgroups ----------------
@@ -428,8 +427,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (mrow) *mrow = 1;
         flag = 1;
         mbar_arrive(smem_u32(&bars.dec));
-        // dO of this tile, loaded only now that the tile is retained
-        if (nret > 0) ok = mbar_wait(smem_u32(&bars.do_empty), (nret - 1) & 1, abortp, a.status);
+        // dO of this tile, loaded only now that the tile is retained.  The
+        // buffer is free: the previous kept tile's dV and dP^T read it, and
+        // every math thread has already seen that dP^T complete (dV runs first).
         if (ok) {
           const uint32_t df = smem_u32(&bars.do_full);
           mbar_expect_tx(df, kTile);
@@ -551,7 +551,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
     // a dO load issued for an abandoned tile must land before the CTA exits
     if (tid == 0 && *abortp && do_issued > 0)
-      mbar_wait(smem_u32(&bars.do_full), (do_issued - 1) & 1, abortp, a.status);
+      mbar_drain(smem_u32(&bars.do_full), (do_issued - 1) & 1, a.status);
     fence_before_sync();
   }
 
