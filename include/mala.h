@@ -308,6 +308,16 @@ size_t mala_decode_noalloc_max_floats(void);
  */
 mala_status mala_device_status(void* stream, int* device_code);
 
+/*
+ * Test hook for failure detection (no counterpart in the paper).  The next
+ * mala_fwd / mala_fwd_varlen call that runs on the tensor-core kernel has one
+ * CTA leave its first K tile unloaded: that CTA's bounded waits expire (after
+ * about 2 s), it gives up without writing its outputs, and bit 1 of the device
+ * status word is set (mala_device_status returns MALA_ERR_TIMEOUT).  Nothing
+ * faults or hangs, and later calls run normally.  One-shot, process-wide.
+ */
+void mala_test_drop_next_load(void);
+
 /* Number of kernels this library has launched in this process (host counter). */
 uint64_t mala_launch_count(void);
 

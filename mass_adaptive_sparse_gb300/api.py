@@ -26,7 +26,7 @@ EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bw
            "mala_fwd_varlen", "mala_bwd_varlen_workspace_size", "mala_bwd_varlen",
            "mala_decode_workspace_size", "mala_decode", "mala_decode_per_head", "mala_decode_varlen",
            "mala_decode_noalloc", "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
-           "mala_last_cuda_error", "mala_cuda_error_string")
+           "mala_test_drop_next_load", "mala_last_cuda_error", "mala_cuda_error_string")
 
 
 class MalaError(RuntimeError):
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.mala_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
         L.mala_launch_count.restype = ctypes.c_uint64
         L.mala_launch_count.argtypes = []
+        L.mala_test_drop_next_load.restype = None
+        L.mala_test_drop_next_load.argtypes = []
         L.mala_last_cuda_error.restype = _i
         L.mala_last_cuda_error.argtypes = []
         L.mala_cuda_error_string.restype = ctypes.c_char_p
@@ -250,6 +252,12 @@ def mala_device_status(stream=None) -> int:
     if rc not in (0, 1, 5):     # OK, a rejected sequence length, an expired wait
         raise MalaError("mala_device_status", rc)
     return code.value
+
+
+def mala_test_drop_next_load():
+    """Failure-detection test hook: the next tensor-core forward call has one
+    CTA's bounded waits expire (see include/mala.h)."""
+    lib().mala_test_drop_next_load()
 
 
 def mala_launch_count() -> int:

@@ -202,21 +202,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, bc);
         tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, bc);
       }
-      int issued = 0;
+      // test hook (failure detection): CTA (0, 0) leaves its first K tile
+      // unloaded, so the waits for it expire and the CTA gives up
+      const bool drop = a.inject != 0 && blockIdx.x == 0 && blockIdx.y == 0;
+      int issued = 0;                     // steps reached (loads issued, or the one dropped)
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % kNK, n = t / kNK;
         if (n > 0 && !mbar_wait(smem_u32(&bars.k_empty[st]), (n - 1) & 1, abortp, a.status)) break;
-        const uint32_t kf = smem_u32(&bars.k_full[st]);
-        const int row = row0 + (jtop - t) * kBlk;
-        mbar_expect_tx(kf, kTile);
-        tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, bc);
-        tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, bc);
+        if (!(drop && t == 0)) {
+          const uint32_t kf = smem_u32(&bars.k_full[st]);
+          const int row = row0 + (jtop - t) * kBlk;
+          mbar_expect_tx(kf, kTile);
+          tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, bc);
+          tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, bc);
+        }
         ++issued;
       }
       // every issued load lands before the CTA can finish
       mbar_drain(smem_u32(&bars.q_full), 0, a.status);
       for (int t = max(0, issued - kNK); t < issued; ++t)
-        mbar_drain(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, a.status);
+        if (!(drop && t == 0)) mbar_drain(smem_u32(&bars.k_full[t % kNK]), (t / kNK) & 1, a.status);
     }
   } else if (warp == 1) {
     // ---------------- V loader ----------------

@@ -18,6 +18,7 @@ using namespace mala;
 __device__ int g_device_status = 0;
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_inject_next{0};         // one-shot failure-detection test hook
 thread_local int g_last_cuda_error = 0;   // cudaError_t of this thread's last MALA_ERR_CUDA
 
 constexpr int kMaxDevices = 64;
@@ -176,7 +177,9 @@ mala_status run_fwd(const void* q, const void* k, const void* v, void* o, float*
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  cudaError_t e = fwd_tc_supported(a) ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
+  const bool tc = fwd_tc_supported(a);
+  if (tc) a.inject = g_inject_next.exchange(0);
+  cudaError_t e = tc ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
   return finish(e, launches);
 }
 
@@ -400,6 +403,8 @@ mala_status mala_device_status(void* stream, int* device_code) {
 }
 
 uint64_t mala_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void mala_test_drop_next_load(void) { g_inject_next.store(1); }
 
 int mala_last_cuda_error(void) { return g_last_cuda_error; }
 

@@ -36,6 +36,7 @@ struct FwdArgs {
   int32_t* counts;      // [B, Hq, Tr] or null
   uint8_t* mask;        // [B, Hq, Tr, Tc] or null
   int* status;          // device status word
+  int inject;           // test hook: CTA (0, 0) drops its first K load (tensor-core kernel)
 };
 
 struct BwdArgs {
