@@ -300,20 +300,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     // on the loaded values waits until the vectors are written, a tile later,
     // so the loads' latency is not paid where they are issued.
     float n_lse = 0.f, n_d = 0.f, n_thr = INFINITY;
-    auto fetch = [&](int t) {
-      const int h = hk * G + t / ni, i = ibot + t % ni;
+    auto fetch = [&](int h, int i) {
       const int q = i * kBlk + r;
       if (q < Lq) {
         const size_t off = (static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + q;
         n_lse = a.lse[off];
         n_d = a.delta[off];
-        n_thr = test ? a.log2_tau - log2f(a.causal ? static_cast<float>(q + 1) : static_cast<float>(Lk))
+        n_thr = test ? a.log2_tau - lg2(a.causal ? static_cast<float>(q + 1) : static_cast<float>(Lk))
                      : -INFINITY;
       } else {
         n_lse = 0.f; n_d = 0.f; n_thr = INFINITY;     // out of range: never kept
       }
     };
-    if (ntiles > 0 && cg == 0) fetch(0);
+    if (ntiles > 0 && cg == 0) fetch(hk * G, ibot);
 
     // Move the finished dQ^T tile (lane = head dim r, columns = queries) out of
     // TMEM, release its region, and add it into the fp32 accumulator with
@@ -351,8 +350,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       return true;
     };
 
-    for (int t = 0; t < ntiles; ++t) {
-      const int h = hk * G + t / ni, i = ibot + t % ni;
+    // tile t = (head h, query block i), heads in turn, query blocks ascending;
+    // carried along rather than divided out of t, which the next vote waits for
+    int h = hk * G, i = ibot;
+    for (int t = 0; t < ntiles; ++t, i = (i + 1 < Tr) ? i + 1 : ibot, h += (i == ibot) ? 1 : 0) {
       const int q0 = i * kBlk;
       if (cg == 0) {
         // lse in log2 units; scale * D (dS = P (scale dP - scale D)); the
@@ -363,7 +364,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         vec_c[r] = n_thr == INFINITY ? INFINITY : (l2 + n_thr) * inv_sl2;
       }
       named_sync(1, kMath);
-      if (cg == 0 && t + 1 < ntiles) fetch(t + 1);
+      if (cg == 0 && t + 1 < ntiles) {
+        const int i1 = (i + 1 < Tr) ? i + 1 : ibot;
+        fetch(i1 == ibot ? h + 1 : h, i1);
+      }
 
       ok = mbar_wait(smem_u32(&bars.s_full), t & 1, abortp, a.status);
       fence_after_sync();
@@ -404,7 +408,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb : nullptr;
       if (tid == 0) {
         head_kept += keep;
-        if (t % ni == ni - 1) {                   // last query block of this head
+        if (i == Tr - 1) {                        // last query block of this head
           if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTc + kb] = head_kept;
           head_kept = 0;
         }
