@@ -249,7 +249,8 @@ def oracle_sample(workload, pool, cores, rank_seed=0, rounds=1):
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    from mass_adaptive_sparse_gb300.replicas import rank_env
+    rank, _, _ = rank_env()
     if rank != 0:
         return
     cores = min(16, os.cpu_count() or 1)
@@ -280,9 +281,8 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from mass_adaptive_sparse_gb300.replicas import Ranks, rank_env, replica_seed
+    rank, world, local = rank_env()
     pool = None
     cores = min(16, os.cpu_count() or 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -302,8 +302,8 @@ def main():
     tau = args.tau
 
     # inputs (seeded per rank: each rank runs its own replica of the workload)
-    xp = synthetic.prefill_inputs(pc, seed=pc.seed + rank)
-    xd = synthetic.decode_inputs(dc, seed=dc.seed + rank)
+    xp = synthetic.prefill_inputs(pc, seed=replica_seed(pc.seed, rank))
+    xd = synthetic.decode_inputs(dc, seed=replica_seed(dc.seed, rank))
     host_in = {n: xp[n].pin_memory() for n in ("q", "k", "v", "do")}
     host_in.update({"qd": xd["q"].pin_memory(), "kc": xd["k"].pin_memory(), "vc": xd["v"].pin_memory()})
     d = {n: t.to(dev) for n, t in host_in.items()}
@@ -335,11 +335,9 @@ def main():
         api.mala_decode(d["qd"], d["kc"], d["vc"], d["od"], d["lsed"], d["ws_d"], block=dc.block,
                         num_splits=dc.num_splits, tau=t, retained_counts=cd)
 
-    def barrier():
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-            torch.cuda.synchronize()
+    ranks = Ranks(dist, dev, torch.cuda.synchronize)
+    barrier = ranks.barrier
+    max_over_ranks = ranks.max
 
     def timed(t, steps):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
@@ -359,13 +357,6 @@ def main():
             ph["decode"].append(e[2].elapsed_time(e[3]))
             ph["step"].append(e[0].elapsed_time(e[3]))
         return {k: statistics.mean(v) for k, v in ph.items()}
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     # --- tau = 1 (the measured configuration) ---
     for _ in range(args.warmup):
@@ -503,7 +494,7 @@ def main():
                            "four streams"}
         del chunks
 
-    if rank != 0:
+    if not ranks.reports:
         if dist is not None:
             dist.destroy_process_group()
         return
@@ -558,7 +549,7 @@ def main():
     secondary = None
     if args.workload == "128k" and not args.no_32k:
         c32 = synthetic.CONFIGS["prefill_32k"]
-        x32 = synthetic.prefill_inputs(c32, seed=c32.seed + rank)
+        x32 = synthetic.prefill_inputs(c32, seed=replica_seed(c32.seed, rank))
         e = {n: x32[n].to(dev) for n in ("q", "k", "v", "do")}
         del x32
         B3, L3, H3, _ = e["q"].shape
