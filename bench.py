@@ -52,6 +52,8 @@ def _args():
     p.add_argument("--no-32k", action="store_true",
                    help="skip the secondary timings (32K prefill, per-head decode)")
     p.add_argument("--sample-seconds", type=float, default=15.0)
+    p.add_argument("--e2e-chunks", type=int, default=8,
+                   help="head chunks of the end-to-end prefill pipeline (rounded to a divisor of the KV heads)")
     return p.parse_args()
 
 
@@ -387,14 +389,15 @@ def main():
         t_dense = timed(0.0, args.steps)
 
     # --- end to end through the public API with host buffers ---
-    # The prefill runs in head chunks (heads are independent), so that one
-    # chunk's inputs arrive while the other computes and one chunk's gradients
-    # leave while the other's backward runs.  Four streams: copies in (in the
-    # order they are needed), compute, the decode (as soon as its cache is in,
-    # alongside the prefill), copies out.
+    # The prefill runs in head chunks (heads are independent; one KV head per
+    # chunk by default), so that later chunks' inputs arrive while earlier ones
+    # compute and earlier chunks' gradients leave while later backwards run:
+    # only the first chunk's inputs and the last chunk's gradients are exposed.
+    # Four streams: copies in (in the order they are needed), compute, the
+    # decode (as soon as its cache is in, alongside the prefill), copies out.
     e2e = None
     if not args.no_e2e:
-        nchunk = 2 if pc.Hkv % 2 == 0 else 1
+        nchunk = math.gcd(max(1, args.e2e_chunks), pc.Hkv)
         hk_per = pc.Hkv // nchunk
         hq_per = hk_per * (pc.H // pc.Hkv)
         chunks = []
