@@ -180,3 +180,33 @@ def test_decode_per_head_128k_full_size_sampled():
     each head deciding alone; sequences 1 and 6 compared with the oracle."""
     cfg = synthetic.CONFIGS["decode_128k"]
     _check(cfg, cfg.N, cfg.B, 1.0, cfg.num_splits, cfg.block, cfg.seed, batches=[1, 6], per_head=True)
+
+
+@pytest.mark.parametrize("splits,kept", [(1, [0, 2, 5]), (2, [1, 2, 5]), (3, [0, 1, 2, 3, 5]),
+                                         (6, [0, 1, 2, 3, 4, 5])])
+def test_decode_split_state_closed_form(splits, kept):
+    """Six 128-key tiles whose keys repeat one score per tile, tau = 3 over
+    N = 768 keys: the closed form of the oracle pin on per-split state, tile
+    for tile (every tile's mass is 128 times the one-key case and so is
+    tau / N's denominator).  Each split starts from its own empty state, so two
+    splits keep tile 1 and skip tile 0 where one pass does the opposite."""
+    scores = [math.log(1.56), math.log(1.25), math.log(2.0), -50.0, -50.0, 0.0]
+    B, G, N, D, blk = 1, 4, 768, 128, 128
+    scale = 1 / math.sqrt(D)
+    q = torch.zeros((B, G, D))
+    q[..., 0] = 16.0
+    k = torch.zeros((B, N, 1, D))
+    for j, s in enumerate(scores):
+        k[0, j * blk:(j + 1) * blk, 0, 0] = s / (16.0 * scale)
+    v = torch.from_numpy(np.random.default_rng(61).standard_normal((B, N, 1, D)))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    q64, k64, v64 = (parity.to64(t) for t in (q, k, v))
+    ref = orc.mala_decode_bhd(q64, k64, v64, scale, 3.0, blk, splits)
+    assert np.flatnonzero(ref["retained"][0, 0]).tolist() == kept
+    o, lse, info = api.decode(q.cuda(), k.cuda(), v.cuda(), 3.0, block=blk, num_splits=splits,
+                              counts=True, mask=True)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 0
+    assert np.flatnonzero(info["mask"].cpu().numpy()[0, 0]).tolist() == kept
+    parity.check_close("o", parity.to64(o), ref["o"], q.dtype)
+    assert np.abs(parity.to64(lse) - ref["lse"]).max() <= parity.LSE_ABS

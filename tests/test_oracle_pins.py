@@ -556,3 +556,49 @@ def test_varlen_equal_lengths_is_the_batched_layout():
     np.testing.assert_array_equal(a["o"], b["o"].reshape(120, 2, 8))
     np.testing.assert_array_equal(a["lse"], b["lse"].transpose(1, 0, 2).reshape(2, 120))
     np.testing.assert_array_equal(a["retained"], b["retained"])
+
+
+# Scores of six one-key tiles (newest last) whose decisions are a closed form
+# with tau / L = 0.5 (tau = 3, L = N = 6), for the split test below.
+SPLIT_SCORES = [math.log(1.56), math.log(1.25), math.log(2.0), -50.0, -50.0, 0.0]
+
+
+def _split_case():
+    s = np.array(SPLIT_SCORES)
+    q = np.array([[1.0, 0.0]])
+    k = np.stack([s, np.zeros(6)], axis=1)
+    v = _rand((6, 3), 95)
+    return q, k, v
+
+
+def test_decode_splits_start_from_empty_state_closed_form():
+    """Each split starts from an empty (m, l) and walks its own tiles newest
+    first (MALA §2.4 and App. A.1, fused decoding execution; Algorithm 1 per
+    split), so more splits can keep a tile that one pass skips and also skip
+    one that it keeps.  §2.4 calls the split's smaller normalizer more
+    conservative; that holds only while the split's normalizer is no larger
+    than the one-pass one, and it is larger once the split has kept a tile
+    that the one pass skipped (tile 1 below).
+
+    Tile masses w = exp(score): tile 5 = 1, tiles 4, 3 = e^-50, tile 2 = 2,
+    tile 1 = 1.25, tile 0 = 1.56; keep iff w_max / Z >= 0.5 (Z = retained
+    mass so far in the split, l = 0 keeps).
+    One split: 5 kept (Z 1); 4, 3 skipped; 2 kept (2/1, Z 3); 1 skipped
+    (1.25/3 = 0.42); 0 kept (1.56/3 = 0.52).
+    Two splits {3,4,5}, {0,1,2}: 5 kept, 4 and 3 skipped; 2 kept (first),
+    1 kept (1.25/2 = 0.63, Z 3.25), 0 skipped (1.56/3.25 = 0.48).
+    Three splits {4,5}, {2,3}, {0,1}: 5 kept, 4 skipped; 3 kept (first), 2 kept;
+    1 kept (first), 0 kept (1.56/1.25).
+    The merged output is the softmax renormalised over the kept keys."""
+    q, k, v = _split_case()
+    w = np.exp(np.array(SPLIT_SCORES))
+    for splits, kept in ((1, [0, 2, 5]), (2, [1, 2, 5]), (3, [0, 1, 2, 3, 5])):
+        r = orc.mala_decode(q, k, v, 1.0, 3.0, 1, splits)
+        assert np.flatnonzero(r.retained).tolist() == kept, splits
+        z = w[kept].sum()
+        np.testing.assert_allclose(r.lse, [math.log(z)], rtol=1e-14)
+        np.testing.assert_allclose(r.o[0], (w[kept, None] * v[kept]).sum(0) / z, rtol=1e-13)
+    # with 6 splits every tile is its split's first, so every tile is kept: dense
+    r6 = orc.mala_decode(q, k, v, 1.0, 3.0, 1, 6)
+    assert r6.retained.all()
+    np.testing.assert_allclose(r6.lse, [math.log(w.sum())], rtol=1e-14)
