@@ -11,7 +11,8 @@ Everything here is written to be checked by eye against the pages:
   §2.2 Eq. (1)-(4) (online forward test, offline backward test, support
   nesting), Algorithm 1 (forward), Algorithm 2 (backward), App. A.1 (fused
   forward/backward/decoding execution, split-KV), App. B Eq. (5)-(10)
-  (omitted-mass bound), App. C.2 (omitted-mass measurement).
+  (omitted-mass bound), App. C.2 (omitted-mass measurement, matched-work
+  allocation controls), §3 Table 1 (the matched-work study).
 * "Why exact attention does not need a quadratic matrix": Method/Mechanism
   (block summary (m, l, u) and the merge identity), Example 1.
 
@@ -48,6 +49,7 @@ __all__ = [
     "mala_decode_bhd", "mala_decode_per_head_bhd",
     "mala_decode_varlen_bhd",
     "omitted_mass", "BORDERLINE_REL",
+    "legal_tiles", "tile_reference_mass", "matched_work_allocation", "top_mass_keep",
 ]
 
 # A tile whose largest contribution ratio lies within this relative distance
@@ -579,3 +581,99 @@ def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_
             retained[b, hk, :t] = r.retained
             margin[b, hk, :t] = r.margin
     return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+
+
+# ---------------------------------------------------------------------------
+# Matched-work allocation controls: §3 "Normalized-Mass Allocation at Matched
+# Work" (Table 1) and App. C.2.  A decision is one (input, head, query block);
+# its candidate regions are the key tiles legal for the block.
+# ---------------------------------------------------------------------------
+
+def legal_tiles(n_q, n_k, bq, bk, causal=True):
+    """[Tr, Tc] bool: tile (i, j) holds at least one legal (query, key) pair."""
+    tr, tc = -(-n_q // bq), -(-n_k // bk)
+    legal = np.zeros((tr, tc), dtype=bool)
+    for i in range(tr):
+        last_row = min(n_q, (i + 1) * bq) - 1
+        for j in range(tc):
+            legal[i, j] = (not causal) or j * bk <= last_row
+    return legal
+
+
+def tile_reference_mass(q, k, scale, bq, bk, causal=True):
+    """Reference mass of every region (App. C.2: the screening-disabled
+    reference "provides the probability mass of every candidate region"): the
+    dense softmax probabilities of tile j's keys summed over the rows of query
+    block i.  Returns [Tr, Tc]; illegal tiles have mass 0, and each block's
+    masses add up to its number of rows."""
+    q, k = _f64(q), _f64(k)
+    nq, nk = q.shape[0], k.shape[0]
+    s = _scores(q, k, scale, np.arange(nq), np.arange(nk), causal)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    tr, tc = -(-nq // bq), -(-nk // bk)
+    mass = np.zeros((tr, tc))
+    for i in range(tr):
+        for j in range(tc):
+            mass[i, j] = p[i * bq:(i + 1) * bq, j * bk:(j + 1) * bk].sum()
+    return mass
+
+
+def matched_work_allocation(counts, scope):
+    """Tiles per decision under one of the diagnostic controls of App. C.2.
+
+    counts [I, H, Tr]: the tiles MALA kept for each decision (input i, head h,
+    query block).  scope:
+      "instance"      - MALA's own count for each decision;
+      "head_position" - one allocation per (head, query block), the average
+                        over inputs (the paper's layer-head-position control;
+                        here there is one layer);
+      "position"      - one allocation per query block, the average over
+                        inputs and heads.
+    A pooled cell's average becomes integers by a rule that looks only at
+    indices: every copy of the cell gets floor(average), and the e copies
+    x with (x - cell) mod n < e get one more, where n is the number of copies
+    and e the cell's remaining units.  So every cell, and the whole, executes
+    exactly MALA's total (the paper's "data-independent integer rounding").
+    Copies are numbered input-major: x = i for head_position, i * H + h for
+    position; cells are numbered h * Tr + query block, or the query block.
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    n_in, n_h, tr = counts.shape
+    out = np.zeros_like(counts)
+    if scope == "instance":
+        return counts.copy()
+    if scope == "head_position":
+        for h in range(n_h):
+            for qb in range(tr):
+                cell, n = h * tr + qb, n_in
+                total = int(sum(counts[i, h, qb] for i in range(n_in)))
+                base, extra = total // n, total % n
+                for i in range(n_in):
+                    out[i, h, qb] = base + (1 if (i - cell) % n < extra else 0)
+        return out
+    if scope == "position":
+        for qb in range(tr):
+            cell, n = qb, n_in * n_h
+            total = int(sum(counts[i, h, qb] for i in range(n_in) for h in range(n_h)))
+            base, extra = total // n, total % n
+            for i in range(n_in):
+                for h in range(n_h):
+                    out[i, h, qb] = base + (1 if (i * n_h + h - cell) % n < extra else 0)
+        return out
+    raise ValueError(f"unknown scope {scope!r}")
+
+
+def top_mass_keep(mass, n_keep, legal):
+    """The controls' selection (App. C.2: "each control retains the
+    highest-mass candidate regions"): for query block i keep the n_keep[i]
+    legal tiles of largest reference mass; equal masses prefer the newer
+    (higher) tile.  Returns [Tr, Tc] bool."""
+    mass = _f64(mass)
+    legal = np.asarray(legal, dtype=bool)
+    keep = np.zeros(mass.shape, dtype=bool)
+    for i in range(mass.shape[0]):
+        cands = sorted((j for j in range(mass.shape[1]) if legal[i, j]), key=lambda j: (-mass[i, j], -j))
+        for j in cands[:int(n_keep[i])]:
+            keep[i, j] = True
+    return keep

@@ -38,6 +38,16 @@ MUTATIONS = [
      "s = np.where(cols[None, :] >= rows[:, None], -np.inf, s)"),
     ("dense D dropped", "ds = p * (dp - dd)", "ds = p * dp"),
     ("lse drops max", "lse[rows] = m + np.log(l)", "lse[rows] = np.log(l)"),
+    ("split state carried over", "    for sp in range(num_splits):\n        m = np.full(g, -np.inf)\n        l = np.zeros(g)\n        u = np.zeros((g, vc.shape[1]))\n",
+     "    m = np.full(g, -np.inf)\n    l = np.zeros(g)\n    u = np.zeros((g, vc.shape[1]))\n    for sp in range(num_splits):\n"),
+    ("region mass transposed", "mass[i, j] = p[i * bq:(i + 1) * bq, j * bk:(j + 1) * bk].sum()",
+     "mass[i, j] = p[j * bk:(j + 1) * bk, i * bq:(i + 1) * bq].sum()"),
+    ("region mass unnormalised", "    p /= p.sum(axis=1, keepdims=True)\n    tr, tc", "    tr, tc"),
+    ("selection keeps lowest mass", "key=lambda j: (-mass[i, j], -j))", "key=lambda j: (mass[i, j], -j))"),
+    ("rounding extra by value", "out[i, h, qb] = base + (1 if (i - cell) % n < extra else 0)",
+     "out[i, h, qb] = base + (1 if counts[i, h, qb] > base else 0)"),
+    ("position pools one head", "total = int(sum(counts[i, h, qb] for i in range(n_in) for h in range(n_h)))",
+     "total = int(sum(counts[i, 0, qb] for i in range(n_in) for h in range(n_h)))"),
 ]
 
 PIN_TESTS = [
@@ -55,6 +65,13 @@ PIN_TESTS = [
     (pins.test_decode_single_split_equals_forward_on_the_head_group, {}),
     (pins.test_uniform_scores_closed_form, {}),
     (pins.test_decode_uniform_scores_closed_form, {}),
+    (pins.test_decode_splits_start_from_empty_state_closed_form, {}),
+    (pins.test_tile_reference_mass_uniform_scores_closed_form, {"causal": True}),
+    (pins.test_tile_reference_mass_blocks_hold_their_rows, {}),
+    (pins.test_top_mass_keep_is_the_best_subset_brute_force, {}),
+    (pins.test_matched_work_allocation_closed_form, {}),
+    (pins.test_matched_work_allocation_matches_work_exactly, {"scope": "head_position"}),
+    (pins.test_matched_work_allocation_matches_work_exactly, {"scope": "position"}),
 ]
 
 

@@ -602,3 +602,75 @@ def test_decode_splits_start_from_empty_state_closed_form():
     r6 = orc.mala_decode(q, k, v, 1.0, 3.0, 1, 6)
     assert r6.retained.all()
     np.testing.assert_allclose(r6.lse, [math.log(w.sum())], rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Matched-work controls (§3 Table 1, App. C.2).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_reference_mass_uniform_scores_closed_form(causal):
+    """q = 0 makes every row's softmax uniform over its legal keys, so a
+    region's mass is a count: sum over the block's rows r of
+    (legal keys of r in the tile) / (legal keys of r)."""
+    nq = nk = 10
+    bq = bk = 4
+    q = np.zeros((nq, 3))
+    k = _rand((nk, 3), 101)
+    got = orc.tile_reference_mass(q, k, 0.7, bq, bk, causal=causal)
+    want = np.zeros((3, 3))
+    for r in range(nq):
+        visible = r + 1 if causal else nk
+        for key in range(visible):
+            want[r // bq, key // bk] += 1.0 / visible
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-15)
+    legal = orc.legal_tiles(nq, nk, bq, bk, causal)
+    assert (got[~legal] == 0).all() and (got[legal] > 0).all()
+
+
+def test_tile_reference_mass_blocks_hold_their_rows():
+    q, k = _rand((37, 8), 102, 2.0), _rand((37, 8), 103, 2.0)
+    mass = orc.tile_reference_mass(q, k, 0.5, 16, 16)
+    np.testing.assert_allclose(mass.sum(axis=1), [16, 16, 5], rtol=1e-13)
+
+
+def test_top_mass_keep_is_the_best_subset_brute_force():
+    """For every block and every n, the kept tiles carry the largest mass any
+    n legal tiles can (checked against all subsets)."""
+    import itertools
+    rng = np.random.default_rng(104)
+    mass = rng.random((4, 6))
+    legal = orc.legal_tiles(4 * 3, 6 * 2, 3, 2)        # a causal pattern of 4 x 6 tiles
+    for n in range(1, 7):
+        keep = orc.top_mass_keep(mass, [n] * 4, legal)
+        for i in range(4):
+            cands = np.flatnonzero(legal[i])
+            best = max(sum(mass[i, list(c)]) for c in itertools.combinations(cands, min(n, len(cands))))
+            assert keep[i].sum() == min(n, len(cands))
+            assert not (keep[i] & ~legal[i]).any()
+            assert mass[i, keep[i]].sum() == pytest.approx(best, rel=1e-14)
+
+
+def test_matched_work_allocation_closed_form():
+    counts = np.array([[[1, 3], [2, 2]], [[1, 4], [3, 2]]])      # [input, head, query block]
+    np.testing.assert_array_equal(orc.matched_work_allocation(counts, "instance"), counts)
+    # (head, block) cells 0..3: totals 2, 7, 5, 4 over 2 inputs; cell 1 gives its
+    # extra unit to input 1, cell 2 to input 0
+    np.testing.assert_array_equal(orc.matched_work_allocation(counts, "head_position"),
+                                  [[[1, 3], [3, 2]], [[1, 4], [2, 2]]])
+    # block cells 0, 1: totals 7 and 11 over 4 copies (x = 2 i + h): base 1 + extra
+    # for x = 0, 1, 2; base 2 + extra for x = 1, 2, 3
+    np.testing.assert_array_equal(orc.matched_work_allocation(counts, "position"),
+                                  [[[2, 2], [2, 3]], [[2, 3], [1, 3]]])
+
+
+@pytest.mark.parametrize("scope", ["head_position", "position"])
+def test_matched_work_allocation_matches_work_exactly(scope):
+    rng = np.random.default_rng(105)
+    legal_per_block = np.arange(1, 9)                         # causal: block i has i + 1 legal tiles
+    counts = rng.integers(1, legal_per_block + 1, size=(5, 3, 8))
+    alloc = orc.matched_work_allocation(counts, scope)
+    axes = (0,) if scope == "head_position" else (0, 1)
+    np.testing.assert_array_equal(alloc.sum(axis=axes), counts.sum(axis=axes))    # per cell, so in total
+    assert (alloc.max(axis=axes) - alloc.min(axis=axes) <= 1).all()              # one allocation per cell
+    assert (alloc >= 1).all() and (alloc <= legal_per_block).all()
