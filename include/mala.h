@@ -98,6 +98,45 @@ mala_status mala_fwd(const void* q, const void* k, const void* v, void* o, float
                      int block_q, int block_k, float tau, float softmax_scale,
                      int32_t* retained_counts, uint8_t* tile_mask, void* stream);
 
+/*
+ * Forward with given tile decisions (the matched-work study of the paper,
+ * §3 "Normalized-Mass Allocation at Matched Work" and App. C.2).
+ *
+ * Softmax attention renormalised over the tiles tile_keep marks: no Eq. (3)
+ * test is made; every legal tile with tile_keep != 0 is kept, every other
+ * tile skipped, in the order mala_fwd visits them.  A row none of whose kept
+ * tiles holds a legal key gets o = 0 and lse = -inf.  Runs on the CUDA cores
+ * (an evaluation path, not the tensor-core kernel).
+ *
+ *  tile_keep [batch, heads_q, ceil(seqlen_q / block_q), ceil(seqlen_k / block_k)]
+ *            uint8, device, required.
+ *  Other arguments as for mala_fwd (tau is not taken).
+ */
+mala_status mala_fwd_forced(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                            int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int causal,
+                            int block_q, int block_k, float softmax_scale, const uint8_t* tile_keep,
+                            int32_t* retained_counts, uint8_t* tile_mask, void* stream);
+
+/*
+ * Reference mass of every (query block, key tile) region (App. C.2: the
+ * screening-disabled reference gives "the probability mass of every candidate
+ * region"):
+ *   region_mass[b, h, i, j] = sum over the valid rows q of query block i and
+ *   the legal keys k of tile j of exp(scale * q . k - lse[b, h, q]).
+ * With lse from a dense (tau = 0) forward each block's masses add up to its
+ * number of valid rows.  Illegal tiles get 0.  CUDA cores.
+ *
+ *  q [batch, seqlen_q, heads_q, head_dim], k [batch, seqlen_k, heads_kv, head_dim]  in_dtype
+ *  lse [batch, heads_q, seqlen_q] float (natural log), input
+ *  region_mass [batch, heads_q, ceil(seqlen_q / block_q), ceil(seqlen_k / block_k)] float, output
+ *  Shape rules as for mala_fwd.
+ */
+mala_status mala_region_mass(const void* q, const void* k, const float* lse, float* region_mass,
+                             int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                             int head_dim, mala_dtype in_dtype, int causal, int block_q, int block_k,
+                             float softmax_scale, void* stream);
+
 /* Bytes of device workspace mala_bwd needs for these sizes. */
 size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
                                int head_dim, mala_dtype in_dtype, mala_dtype grad_dtype);

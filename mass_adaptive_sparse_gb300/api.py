@@ -26,7 +26,8 @@ EXPORTS = ("mala_status_string", "mala_fwd", "mala_bwd_workspace_size", "mala_bw
            "mala_fwd_varlen", "mala_bwd_varlen_workspace_size", "mala_bwd_varlen",
            "mala_decode_workspace_size", "mala_decode", "mala_decode_per_head", "mala_decode_varlen",
            "mala_decode_noalloc", "mala_decode_noalloc_max_floats", "mala_device_status", "mala_launch_count",
-           "mala_test_drop_next_load", "mala_last_cuda_error", "mala_cuda_error_string")
+           "mala_test_drop_next_load", "mala_last_cuda_error", "mala_cuda_error_string",
+           "mala_fwd_forced", "mala_region_mass")
 
 
 class MalaError(RuntimeError):
@@ -51,6 +52,10 @@ def lib() -> ctypes.CDLL:
         L.mala_status_string.argtypes = [_i]
         L.mala_fwd.restype = _i
         L.mala_fwd.argtypes = [_vp] * 5 + [_i] * 6 + [_i, _i, _i, _i, _i, _f, _f, _vp, _vp, _vp]
+        L.mala_fwd_forced.restype = _i
+        L.mala_fwd_forced.argtypes = [_vp] * 5 + [_i] * 6 + [_i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp]
+        L.mala_region_mass.restype = _i
+        L.mala_region_mass.argtypes = [_vp] * 4 + [_i] * 6 + [_i, _i, _i, _i, _f, _vp]
         L.mala_bwd_workspace_size.restype = _sz
         L.mala_bwd_workspace_size.argtypes = [_i] * 8
         L.mala_bwd.restype = _i
@@ -134,6 +139,31 @@ def mala_fwd(q, k, v, o, lse, *, causal=True, block=128, tau=1.0, softmax_scale=
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lk, Hq, Hkv, D, _dt(q), _dt(o),
         int(causal), block, block, float(tau), _scale(D, softmax_scale),
         _ptr(retained_counts), _ptr(tile_mask), _stream(stream)))
+
+
+def mala_fwd_forced(q, k, v, o, lse, tile_keep, *, causal=True, block=128, softmax_scale=None,
+                    retained_counts=None, tile_mask=None, stream=None):
+    """Forward over the tiles `tile_keep` (uint8 [B, Hq, Tr, Tc]) marks, no test."""
+    B, Lq, Hq, D = q.shape
+    Lk, Hkv = k.shape[1], k.shape[2]
+    if tile_keep.dtype != torch.uint8 or tile_keep.shape != (B, Hq, -(-Lq // block), -(-Lk // block)):
+        raise ValueError("tile_keep must be uint8 [B, Hq, ceil(Lq / block), ceil(Lk / block)]")
+    _check("mala_fwd_forced", lib().mala_fwd_forced(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lk, Hq, Hkv, D, _dt(q), _dt(o),
+        int(causal), block, block, _scale(D, softmax_scale), _ptr(tile_keep),
+        _ptr(retained_counts), _ptr(tile_mask), _stream(stream)))
+
+
+def mala_region_mass(q, k, lse, region_mass, *, causal=True, block=128, softmax_scale=None, stream=None):
+    """region_mass (fp32 [B, Hq, Tr, Tc]) = each (query block, key tile) region's
+    softmax mass under the row log-normalisers `lse`, summed over the block's rows."""
+    B, Lq, Hq, D = q.shape
+    Lk, Hkv = k.shape[1], k.shape[2]
+    if region_mass.dtype != torch.float32 or region_mass.shape != (B, Hq, -(-Lq // block), -(-Lk // block)):
+        raise ValueError("region_mass must be float32 [B, Hq, ceil(Lq / block), ceil(Lk / block)]")
+    _check("mala_region_mass", lib().mala_region_mass(
+        _ptr(q), _ptr(k), _ptr(lse), _ptr(region_mass), B, Lq, Lk, Hq, Hkv, D, _dt(q), int(causal),
+        block, block, _scale(D, softmax_scale), _stream(stream)))
 
 
 def mala_bwd_workspace_size(q, k, grad_dtype):

@@ -158,7 +158,8 @@ bool workspace_ok(const void* workspace, size_t workspace_bytes, size_t need) {
 mala_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu,
                     int batch, int seqlen_q, int seqlen_k, int lmax, int heads_q, int heads_kv, int head_dim,
                     int in_dtype, int out_dtype, int causal, int block_q, int block_k, float tau,
-                    float softmax_scale, int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+                    float softmax_scale, int32_t* retained_counts, uint8_t* tile_mask, void* stream,
+                    const uint8_t* force = nullptr) {
   if (!q || !k || !v || !o || !lse) return MALA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return MALA_ERR_INVALID_ARG;
@@ -175,9 +176,11 @@ mala_status run_fwd(const void* q, const void* k, const void* v, void* o, float*
   a.tau = tau; a.log2_tau = tau > 0.f ? std::log2(tau) : 0.f;
   a.scale_log2 = softmax_scale * kLog2e;
   a.counts = retained_counts; a.mask = tile_mask; a.status = status;
+  a.force = force;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int launches = 0;
-  const bool tc = fwd_tc_supported(a);
+  // forced decisions run on the CUDA-core kernel (an evaluation path)
+  const bool tc = force == nullptr && fwd_tc_supported(a);
   if (tc) a.inject = g_inject_next.exchange(0);
   cudaError_t e = tc ? launch_fwd_tc(a, s, &launches) : launch_fwd_simt(a, s, &launches);
   return finish(e, launches);
@@ -272,6 +275,39 @@ mala_status mala_fwd_varlen(const void* q, const void* k, const void* v, void* o
   return run_fwd(q, k, v, o, lse, cu_seqlens, batch, total_tokens, total_tokens, max_seqlen, heads_q, heads_kv,
                  head_dim, in_dtype, out_dtype, causal, block_q, block_k, tau, softmax_scale, retained_counts,
                  tile_mask, stream);
+}
+
+mala_status mala_fwd_forced(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                            int head_dim, mala_dtype in_dtype, mala_dtype out_dtype, int causal,
+                            int block_q, int block_k, float softmax_scale, const uint8_t* tile_keep,
+                            int32_t* retained_counts, uint8_t* tile_mask, void* stream) {
+  if (!tile_keep) return MALA_ERR_INVALID_ARG;
+  return run_fwd(q, k, v, o, lse, nullptr, batch, seqlen_q, seqlen_k, seqlen_q, heads_q, heads_kv, head_dim,
+                 in_dtype, out_dtype, causal, block_q, block_k, 0.f, softmax_scale, retained_counts, tile_mask,
+                 stream, tile_keep);
+}
+
+mala_status mala_region_mass(const void* q, const void* k, const float* lse, float* region_mass,
+                             int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,
+                             int head_dim, mala_dtype in_dtype, int causal, int block_q, int block_k,
+                             float softmax_scale, void* stream) {
+  if (!q || !k || !lse || !region_mass) return MALA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(region_mass) & 3u))
+    return MALA_ERR_INVALID_ARG;
+  mala_status st = check_prefill(batch, seqlen_q, seqlen_k, heads_q, heads_kv, head_dim, in_dtype, in_dtype,
+                                 causal, block_q, block_k, 0.f, softmax_scale);
+  if (st != MALA_OK) return st;
+  FwdArgs a{};
+  a.q = q; a.k = k; a.lse = const_cast<float*>(lse); a.region_mass = region_mass;
+  a.B = batch; a.Lq = seqlen_q; a.Lk = seqlen_k; a.Hq = heads_q; a.Hkv = heads_kv; a.D = head_dim;
+  a.Lmax = seqlen_q;
+  a.in_dt = in_dtype; a.out_dt = in_dtype; a.causal = causal; a.blk = block_q;
+  a.scale_log2 = softmax_scale * kLog2e;
+  int launches = 0;
+  cudaError_t e = launch_region_mass(a, static_cast<cudaStream_t>(stream), &launches);
+  return finish(e, launches);
 }
 
 size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_q, int heads_kv,

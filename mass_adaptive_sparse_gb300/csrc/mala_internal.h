@@ -37,6 +37,9 @@ struct FwdArgs {
   uint8_t* mask;        // [B, Hq, Tr, Tc] or null
   int* status;          // device status word
   int inject;           // test hook: CTA (0, 0) drops its first K load (tensor-core kernel)
+  const uint8_t* force; // [B, Hq, Tr, Tc] tile decisions to follow instead of the test, or null
+                        // (CUDA-core forward only)
+  float* region_mass;   // [B, Hq, Tr, Tc] output of the region-mass kernel (lse is then an input)
 };
 
 struct BwdArgs {
@@ -110,6 +113,8 @@ cudaError_t launch_decode_simt(const DecArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_decode_merge(const DecArgs& a, cudaStream_t s, int* launches);
+// Reference mass of every (query block, key tile) region from the final lse.
+cudaError_t launch_region_mass(const FwdArgs& a, cudaStream_t s, int* launches);
 
 // Tensor-core (tcgen05) kernels: bf16 inputs, head_dim 128, 128 x 128 tiles.
 bool fwd_tc_supported(const FwdArgs& a);

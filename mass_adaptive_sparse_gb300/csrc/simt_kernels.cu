@@ -115,7 +115,9 @@ fwd_simt_kernel(const FwdArgs a) {
     bool keep_row = false;
     if (row_valid && mt > -INFINITY)
       keep_row = !test || l == 0.f || !(mt - m - log2f(l) < thr);
-    const int keep = __syncthreads_or(keep_row);
+    int keep = __syncthreads_or(keep_row);
+    // forced decisions: the given tile set, with no test (matched-work controls)
+    if (a.force != nullptr) keep = a.force[((static_cast<size_t>(b) * a.Hq + h) * mTr + qb) * mTc + j] != 0;
     if (a.mask != nullptr && tid == 0)
       a.mask[((static_cast<size_t>(b) * a.Hq + h) * mTr + qb) * mTc + j] = keep ? 1 : 0;
     if (!keep) continue;
@@ -142,12 +144,79 @@ fwd_simt_kernel(const FwdArgs a) {
   }
   if (row_valid) {
     Tout* op = static_cast<Tout*>(a.o) + ((static_cast<size_t>(bc) * a.Lq + row0 + qrow) * a.Hq + h) * D;
-    const float inv = 1.f / l;
+    // l = 0 only when forced decisions keep none of the row's keys: o = 0, lse = -inf
+    const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int c = 0; c < 32; ++c) st(op + c * TPR + part, acc[c] * inv);
-    if (part == 0) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m + log2f(l)) * kLn2;
+    if (part == 0)
+      a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
   }
   if (a.counts != nullptr && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTr + qb] = kept;
+}
+
+// ---------------------------------------------------------------------------
+// Reference region mass (the matched-work study of the MALA paper, App. C.2):
+// for query block qb and key tile j, the sum over the block's valid rows and
+// the tile's legal keys of exp(s - lse), lse being the row's final
+// log-normaliser.  One CTA per (query block, query head, batch), one tile at a
+// time from the diagonal down; illegal tiles get 0.
+// ---------------------------------------------------------------------------
+template <typename Tin, int D, int BLK>
+__global__ void __launch_bounds__(BLK * (D / 32))
+region_mass_kernel(const FwdArgs a) {
+  constexpr int TPR = D / 32;
+  constexpr int NT = BLK * TPR;
+  extern __shared__ float smem[];
+  float* Ks = smem;                           // [BLK][D]
+  __shared__ float tile_sum;
+
+  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int Lq = a.Lq, Lk = a.Lk;
+  const int Tr = (Lq + BLK - 1) / BLK, Tc = (Lk + BLK - 1) / BLK;
+  if (qb >= Tr) return;
+  const int hk = h / (a.Hq / a.Hkv);
+  const int tid = threadIdx.x, r = tid / TPR, part = tid % TPR;
+  const int qrow = qb * BLK + r;
+  const bool row_valid = qrow < Lq;
+  const Tin* qg = static_cast<const Tin*>(a.q);
+  const Tin* kg = static_cast<const Tin*>(a.k);
+
+  float qv[32];
+  {
+    const Tin* qp = qg + ((static_cast<size_t>(b) * Lq + (row_valid ? qrow : 0)) * a.Hq + h) * D;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) qv[c] = row_valid ? ld(qp + c * TPR + part) * a.scale_log2 : 0.f;
+  }
+  const float lse2 = row_valid ? a.lse[(static_cast<size_t>(b) * a.Hq + h) * Lq + qrow] * kLog2e : 0.f;
+  const int jtop = a.causal ? min(Tc - 1, (min(Lq, qb * BLK + BLK) - 1) / BLK) : Tc - 1;
+  float* out = a.region_mass + ((static_cast<size_t>(b) * a.Hq + h) * Tr + qb) * Tc;
+  for (int j = jtop + 1 + tid; j < Tc; j += NT) out[j] = 0.f;
+
+  for (int j = jtop; j >= 0; --j) {
+    const int k0 = j * BLK;
+    __syncthreads();
+    for (int idx = tid; idx < BLK * D; idx += NT) {
+      const int kr = idx / D, c = idx % D, key = k0 + kr;
+      Ks[idx] = key < Lk ? ld(kg + ((static_cast<size_t>(b) * Lk + key) * a.Hkv + hk) * D + c) : 0.f;
+    }
+    if (tid == 0) tile_sum = 0.f;
+    __syncthreads();
+    float ps = 0.f;
+    for (int kr = 0; kr < BLK; ++kr) {
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) s = fmaf(qv[c], Ks[kr * D + c * TPR + part], s);
+      s = row_sum<TPR>(s);
+      const int key = k0 + kr;
+      const bool legal = row_valid && key < Lk && (!a.causal || key <= qrow);
+      if (legal && part == 0) ps += exp2f(s - lse2);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(kFull, ps, off);
+    if ((tid & 31) == 0) atomicAdd(&tile_sum, ps);
+    __syncthreads();
+    if (tid == 0) out[j] = tile_sum;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -544,6 +613,17 @@ cudaError_t fwd_pick(const FwdArgs& a, cudaStream_t s) {
   return fwd_go<Tin, Tout, 128, 128>(a, s);
 }
 
+template <typename Tin, int D, int BLK>
+cudaError_t mass_go(const FwdArgs& a, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(BLK) * D * sizeof(float);
+  auto kern = region_mass_kernel<Tin, D, BLK>;
+  cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Lq + BLK - 1) / BLK, a.Hq, a.B);
+  kern<<<grid, BLK * (D / 32), smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename Tin, typename Tg, int D, int BLK>
 cudaError_t bwd_go(const BwdArgs& a, cudaStream_t s) {
   const size_t smem = bwd_simt_smem(a.in_dt, D, BLK);
@@ -602,6 +682,16 @@ size_t bwd_simt_smem(int in_dt, int D, int blk) {
   bytes = (bytes + 15) / 16 * 16;
   bytes += (static_cast<size_t>(blk) * (blk + 1) + 3 * blk) * sizeof(float);
   return bytes;
+}
+
+cudaError_t launch_region_mass(const FwdArgs& a, cudaStream_t s, int* launches) {
+  ++*launches;
+  if (a.in_dt == kBF16) {
+    if (a.D == 64) return a.blk == 64 ? mass_go<__nv_bfloat16, 64, 64>(a, s) : mass_go<__nv_bfloat16, 64, 128>(a, s);
+    return a.blk == 64 ? mass_go<__nv_bfloat16, 128, 64>(a, s) : mass_go<__nv_bfloat16, 128, 128>(a, s);
+  }
+  if (a.D == 64) return a.blk == 64 ? mass_go<float, 64, 64>(a, s) : mass_go<float, 64, 128>(a, s);
+  return a.blk == 64 ? mass_go<float, 128, 64>(a, s) : mass_go<float, 128, 128>(a, s);
 }
 
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s, int* launches) {

@@ -7,7 +7,11 @@ from here.
 The generator plants, for each query position i, a few "target" keys drawn
 uniformly from its causal prefix [0, i] and sets
     q_i = A * mean(k_targets) + N(0, 1)
-so each query row has a few large scores above a Gaussian background.  Two
+so each query row has a few large scores above a Gaussian background.  With
+target_rows = G > 1, each group of G consecutive rows shares one draw of
+targets (over the group's first row's prefix), which makes the peaks coherent
+across a query block.  Per-head amplitudes are drawn from the input's seed, or
+from amp_seed when it is set (the same heads for every input).  Two
 logit biases are folded into the last head-dim coordinate, because the
 operator takes only q, k and v:
     q[..., d-1] = 16,   k[j, d-1] = (sink * [j == 0] + c * j) * sqrt(d) / 16,
@@ -76,6 +80,8 @@ class PrefillConfig:
     recency: float    # c in the bias -c (i - j)
     taus: tuple = (1.0,)
     seed: int = 0
+    target_rows: int = 1          # consecutive query rows that share their target keys
+    amp_seed: int | None = None   # draw the per-head amplitudes from this seed (fixed across inputs)
 
 
 @dataclass
@@ -103,6 +109,10 @@ CONFIGS = {
     "prefill_8k": PrefillConfig("prefill_8k", 1, 16, 16, 8192, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.002, (1.0,), 1002),
     "prefill_32k": PrefillConfig("prefill_32k", 1, 8, 8, 32768, 128, 128, torch.bfloat16, 3, (2.0, 4.0, 8.0), 3.0, 0.002, (1.0, 0.0), 1003),
     "prefill_128k": PrefillConfig("prefill_128k", 1, 8, 8, 131072, 128, 128, torch.bfloat16, 5, (6.0,), 3.0, 1e-4, (1.0, 0.0), 1004),
+    # the matched-work study's inputs: 8K tokens, 8 heads of fixed amplitudes 2 / 4 / 8,
+    # targets shared by each 128-row query block
+    "study_8k": PrefillConfig("study_8k", 1, 8, 8, 8192, 128, 128, torch.bfloat16, 3, (2.0, 4.0, 8.0), 3.0, 0.002,
+                              (1.0,), 1006, target_rows=128, amp_seed=1007),
     "decode_128k": DecodeConfig("decode_128k", 8, 32, 8, 131072, 128, 128, 16, torch.bfloat16, 4, 6.0, (1.0, 0.0), 1005),
 }
 
@@ -127,15 +137,20 @@ def prefill_inputs(cfg: PrefillConfig, L: int | None = None, seed: int | None = 
     s_k, s_v, s_noise, s_tgt, s_amp, s_do = ss.spawn(6)
     k = _normal(s_k, B * L * Hkv * d).reshape(B, L, Hkv, d)
     v = _normal(s_v, B * L * Hkv * d).reshape(B, L, Hkv, d)
-    amp = _head_amplitudes(np.random.default_rng(s_amp), cfg.amplitude, H)
+    amp_rng = np.random.default_rng(s_amp if cfg.amp_seed is None else np.random.SeedSequence(cfg.amp_seed))
+    amp = _head_amplitudes(amp_rng, cfg.amplitude, H)
     q = _normal(s_noise, B * L * H * d).reshape(B, L, H, d)
     rng_t = np.random.default_rng(s_tgt)
     grp = H // Hkv
     pos = np.arange(L)
     for b in range(B):
         for h in range(H):
-            # n_targets keys per query, uniform over the causal prefix [0, i]
-            tgt = np.floor(rng_t.random((L, cfg.n_targets)) * (pos[:, None] + 1)).astype(np.int64)
+            # n_targets keys per query, uniform over the causal prefix [0, i]; a group
+            # of target_rows consecutive rows shares one draw over its first row's prefix
+            g = cfg.target_rows
+            first = pos[::g]
+            tgt = np.floor(rng_t.random((len(first), cfg.n_targets)) * (first[:, None] + 1)).astype(np.int64)
+            tgt = np.repeat(tgt, g, axis=0)[:L]
             kk = k[b, :, h // grp, : d - 1]
             mean_t = kk[tgt].mean(axis=1)
             q[b, :, h, : d - 1] += (amp[h] * mean_t).astype(np.float32)
