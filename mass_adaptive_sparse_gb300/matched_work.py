@@ -164,7 +164,9 @@ def decision_metrics(o, lse, o_ref, lse_ref, block):
 
 
 def run(ds: list, block: int) -> dict:
-    """The four policies over the inputs' decisions; returns one row per policy."""
+    """The four policies over the inputs' decisions; returns one row per
+    policy (and the kernels' times).  The sequences of a batch count as heads
+    of one input."""
     dev = ds[0].counts.device
     B, H, tr = ds[0].counts.shape
     L = ds[0].inputs["q"].shape[1]
@@ -186,8 +188,9 @@ def run(ds: list, block: int) -> dict:
             a, b = decision_metrics(o, lse, d.o_ref, d.lse_ref, block)
             om.append(a.flatten())
             er.append(b.flatten())
-            if pol != "mala":
-                assert torch.equal(keep.sum(-1, dtype=torch.int64).cpu(), torch.from_numpy(n[i].reshape(B, H, tr)))
+            if pol != "mala" and not torch.equal(keep.sum(-1, dtype=torch.int64).cpu(),
+                                                 torch.from_numpy(n[i].reshape(B, H, tr))):
+                raise RuntimeError(f"{pol}: the selection does not run the allocated number of tiles")
         om, er = torch.cat(om).cpu().numpy(), torch.cat(er).cpu().numpy()
         slots = float((n * block * rows_per_block[None, None, :]).sum() / (len(ds) * B * H * L))
         out[pol] = {"policy": LABELS[pol], "tiles": int(n.sum()), "mean_slots": slots,
