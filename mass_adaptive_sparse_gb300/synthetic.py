@@ -58,6 +58,14 @@ def _normal(seed_seq: np.random.SeedSequence, n: int) -> np.ndarray:
     return out
 
 
+def rademacher(shape: tuple, seed: int, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """A deterministic Rademacher probe: independent +-1 entries of `shape`
+    from `seed` (exact in every float dtype)."""
+    rng = np.random.default_rng(np.random.SeedSequence(seed))
+    signs = rng.integers(0, 2, size=int(np.prod(shape)), dtype=np.int8) * 2 - 1
+    return torch.from_numpy(signs.astype(np.float32).reshape(shape)).to(dtype)
+
+
 def _round(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
     """Round-to-nearest-even into ``dtype`` (torch's conversion)."""
     return torch.from_numpy(np.ascontiguousarray(x)).to(dtype)

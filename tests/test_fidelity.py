@@ -3,20 +3,19 @@ App. C.3), on the CPU."""
 import numpy as np
 import torch
 
-from mass_adaptive_sparse_gb300 import fidelity as fd
+from mass_adaptive_sparse_gb300 import fidelity as fd, synthetic
 
 
 def test_relative_errors_closed_form():
-    """Every row off by a vector of 2% of its norm; one head's tensor off by
-    a tenth of itself."""
+    """One head's tensor off by a tenth of itself, another's by a vector of 2%
+    of its norm in every row (so 2% of the whole)."""
     B, L, H, D = 2, 7, 3, 5
     ref = torch.randn(B, L, H, D, dtype=torch.float64)
-    u = torch.randn(B, L, H, D, dtype=torch.float64)
+    u = torch.randn(B, L, D, dtype=torch.float64)
     u = u / torch.linalg.vector_norm(u, dim=-1, keepdim=True)
-    x = ref + 0.02 * torch.linalg.vector_norm(ref, dim=-1, keepdim=True) * u
-    rows = fd.rel_rows(x, ref)
-    assert rows.shape == (B, H, L)
-    np.testing.assert_allclose(rows.numpy(), 0.02, rtol=1e-12)
+    x = ref.clone()
+    x[:, :, 2] += 0.02 * torch.linalg.vector_norm(ref[:, :, 2], dim=-1, keepdim=True) * u
+    np.testing.assert_allclose(fd.rel_heads(x, ref).numpy()[:, 2], 0.02, rtol=1e-12)
     y = ref.clone()
     y[:, :, 1] *= 1.1
     np.testing.assert_allclose(fd.rel_heads(y, ref).numpy(), [[0, 0.1, 0]] * B, atol=1e-15, rtol=1e-12)
@@ -30,3 +29,11 @@ def test_slots_and_pooling():
     p = fd.pool(states)
     assert p["a"]["mean"] == 2.0
     assert p["a"]["p95"] == np.percentile([1.0, 2.0, 3.0], 95)
+
+
+def test_rademacher_probe():
+    a = synthetic.rademacher((3, 1000), 5)
+    assert set(a.float().unique().tolist()) == {-1.0, 1.0}
+    assert torch.equal(a, synthetic.rademacher((3, 1000), 5))
+    assert not torch.equal(a, synthetic.rademacher((3, 1000), 6))
+    assert abs(float(a.float().mean())) < 0.1
