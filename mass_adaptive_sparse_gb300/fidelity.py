@@ -100,7 +100,7 @@ def study(workload: str = "study_8k", lengths=(1024, 2048, 4096, 8192), n_inputs
 def main():
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--workload", default="study_8k", choices=sorted(synthetic.CONFIGS))
-    p.add_argument("--lengths", default="1024,2048,4096,8192")
+    p.add_argument("--lengths", default="1024,2048,4096,8192,16384,32768")
     p.add_argument("--inputs", type=int, default=2)
     p.add_argument("--tau", type=float, default=1.0)
     args = p.parse_args()
