@@ -117,3 +117,24 @@ def test_decode_varlen_rejects_missing_or_misaligned_lengths(lib):
     bad = list(shape)
     bad[2], bad[3] = 48, 3                      # group of 16
     assert lib.mala_decode_varlen(*args, FAKE, *bad) == 2
+
+
+def test_forced_forward_rejects_bad_arguments(lib):
+    shape = [1, 256, 256, 2, 2, 128, 0, 1, 1, 128, 128, 0.088]
+    assert lib.mala_fwd_forced(*[FAKE] * 5, *shape, None, None, None, None) == 1        # no tile set
+    assert lib.mala_fwd_forced(None, *[FAKE] * 4, *shape, FAKE, None, None, None) == 1
+    bad = list(shape)
+    bad[5] = 96                                                                        # head_dim
+    assert lib.mala_fwd_forced(*[FAKE] * 5, *bad, FAKE, None, None, None) == 2
+
+
+def test_region_mass_rejects_bad_arguments(lib):
+    shape = [1, 256, 256, 2, 2, 128, 0, 1, 128, 128, 0.088]
+    assert lib.mala_region_mass(FAKE, FAKE, None, FAKE, *shape, None) == 1
+    assert lib.mala_region_mass(FAKE, FAKE, ctypes.c_void_p(0x10002), FAKE, *shape, None) == 1
+    bad = list(shape)
+    bad[3], bad[4] = 3, 2                                                              # Hq % Hkv
+    assert lib.mala_region_mass(FAKE, FAKE, FAKE, FAKE, *bad, None) == 1
+    bad = list(shape)
+    bad[8], bad[9] = 64, 128                                                           # block_q != block_k
+    assert lib.mala_region_mass(FAKE, FAKE, FAKE, FAKE, *bad, None) == 2
