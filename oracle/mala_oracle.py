@@ -22,7 +22,7 @@ Conventions (one head at a time; the *_bshd wrappers loop over batch/heads):
   Natural exp/log throughout (§2.1).  Zero-based positions; causal prefill
   means key k is visible to query q iff k <= q, so L_q = q + 1 (§2.1).
 
-Readings of points the pages leave open (each also listed in the design notes):
+Readings of points the pages leave open:
   * only key blocks with at least one legal entry for the query block are
     visited (Algorithm 1 loops over all j; App. A.1 says "legal key blocks");
   * rows (or entries) that are out of range or fully masked in a tile do not
@@ -48,7 +48,7 @@ __all__ = [
     "mala_forward_bshd", "mala_backward_bshd", "mala_forward_varlen", "mala_backward_varlen",
     "mala_decode_bhd", "mala_decode_per_head_bhd",
     "mala_decode_varlen_bhd",
-    "omitted_mass", "BORDERLINE_REL",
+    "omitted_mass", "BORDERLINE_REL", "is_borderline",
     "legal_tiles", "tile_reference_mass", "matched_work_allocation", "top_mass_keep",
 ]
 
@@ -56,6 +56,28 @@ __all__ = [
 # of tau/L_q is "borderline": fp32 and fp64 evaluations may legitimately
 # decide it differently.
 BORDERLINE_REL = 1e-3
+
+
+def is_borderline(margin):
+    """True where a tile's largest contribution ratio lies within
+    BORDERLINE_REL (relative) of the threshold: margin is the log of
+    ratio / (tau / L_q), so the band is |exp(margin) - 1| <= BORDERLINE_REL.
+    Infinite margins (l = 0, always retained) and NaN (not tested) are not
+    borderline."""
+    m = np.asarray(margin, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.isfinite(m) & (np.abs(np.expm1(m)) <= BORDERLINE_REL)
+
+
+def _follow(skip, margin, forced):
+    """Forced-decision replay: at a borderline tile, where an fp32 and an fp64
+    evaluation of the same test may legitimately disagree, take the given
+    decision (forced = keep) instead of this run's own; elsewhere keep the
+    test's.  Returns (skip, overridden)."""
+    if forced is None or not is_borderline(margin):
+        return skip, False
+    follow_skip = not bool(forced)
+    return follow_skip, follow_skip != skip
 
 
 def _f64(x):
@@ -161,13 +183,15 @@ class MalaForward:
     retained: np.ndarray   # [Tr, Tc] bool: post-score path executed
     legal: np.ndarray      # [Tr, Tc] bool: tile has >= 1 legal entry (visited)
     margin: np.ndarray     # [Tr, Tc] max over rows of (log-ratio - log(tau/L)); skip iff < 0
+    overridden: np.ndarray = None  # [Tr, Tc] bool: borderline tiles where a forced decision
+                                   # differed from this run's own test (replay only)
 
 
 def _log_threshold(tau, lq):
     return math.log(tau) - np.log(lq)
 
 
-def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
+def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None, forced=None):
     """MALA forward for one head (Algorithm 1).
 
     For each query block, legal key blocks are visited from the diagonal
@@ -178,6 +202,14 @@ def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
     (m, l, O) untouched; a retained one takes the standard online-softmax
     update.  Finalisation: O /= l and lse = m + log(l).
     ``query_blocks`` restricts the work to a subset of blocks (others stay 0).
+
+    ``forced`` ([Tr, Tc] bool, e.g. another implementation's tile mask) makes
+    this a forced-decision replay: at a tile whose margin, measured on this
+    run's own (m, l), is borderline (``is_borderline``), the given decision is
+    taken instead of the test's; every other tile is decided by Eq. 3 as
+    usual.  Because each later test reads the (m, l) that the earlier
+    decisions produced (Algorithm 1), the replay is the oracle's result for
+    the path on which every borderline tile went the given way.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     if tau < 0 or not np.isfinite(tau):
@@ -190,6 +222,7 @@ def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
     retained = np.zeros((tr, tc), dtype=bool)
     legal = np.zeros((tr, tc), dtype=bool)
     margin = np.full((tr, tc), np.nan)
+    overridden = np.zeros((tr, tc), dtype=bool)
     blocks = range(tr) if query_blocks is None else query_blocks
     for i in blocks:
         rows = np.arange(i * bq, min(nq, (i + 1) * bq))
@@ -210,7 +243,9 @@ def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
                     ratio = np.where(l > 0, mt - m - np.log(np.where(l > 0, l, 1.0)), np.inf)
                 gap = (ratio - thr)[has]
                 margin[i, j] = gap.max()
-                if np.all(gap < 0):
+                skip, overridden[i, j] = _follow(bool(np.all(gap < 0)), margin[i, j],
+                                                 None if forced is None else forced[i, j])
+                if skip:
                     continue                      # skip block (i, j)
             retained[i, j] = True
             # online-softmax update; rows without a legal key here keep their state
@@ -225,7 +260,7 @@ def mala_forward(q, k, v, scale, tau, bq, bk, causal=True, query_blocks=None):
             m = m_new
         o[rows] = acc / l[:, None]
         lse[rows] = m + np.log(l)
-    return MalaForward(o, lse, retained, legal, margin)
+    return MalaForward(o, lse, retained, legal, margin, overridden)
 
 
 # ---------------------------------------------------------------------------
@@ -240,9 +275,10 @@ class MalaBackward:
     retained: np.ndarray   # [Tr, Tc] bool (indexed [query block, key block])
     legal: np.ndarray
     margin: np.ndarray     # max over valid entries of (S - lse - log(tau/L)); skip iff < 0
+    overridden: np.ndarray = None  # borderline tiles where a forced decision differed (replay only)
 
 
-def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=None):
+def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=None, forced=None):
     """MALA backward for one head (Algorithm 2), key-major.
 
     For each key block j, the query blocks i with a legal entry are visited in
@@ -252,7 +288,10 @@ def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=No
     dS = P o (dP - rowsum(O o dO)), dV += P dO, dK += dS Q, dQ += dS^T K,
     with the softmax scale carried onto dQ and dK (gradients are w.r.t. the
     unscaled q and k).  ``tiles`` (a predicate on (i, j)) restricts the work
-    to a subset of tiles, for sampled checks at large sizes.
+    to a subset of tiles, for sampled checks at large sizes.  ``forced``
+    ([Tr, Tc] bool) replays given decisions at borderline tiles, as in
+    ``mala_forward``; here each test reads only the fixed lse, so a followed
+    decision changes no other tile's.
     """
     q, k, v, o, do, lse = (_f64(x) for x in (q, k, v, o, do, lse))
     if tau < 0 or not np.isfinite(tau):
@@ -267,6 +306,7 @@ def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=No
     retained = np.zeros((tr, tc), dtype=bool)
     legal = np.zeros((tr, tc), dtype=bool)
     margin = np.full((tr, tc), np.nan)
+    overridden = np.zeros((tr, tc), dtype=bool)
     for j in range(tc):
         cols = np.arange(j * bk, min(nk, (j + 1) * bk))
         for i in range(tr):
@@ -282,7 +322,9 @@ def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=No
                 thr = _log_threshold(tau, lvis[rows])
                 gap = (st - lse[rows][None, :] - thr[None, :])[valid]
                 margin[i, j] = gap.max()
-                if np.all(gap < 0):
+                skip, overridden[i, j] = _follow(bool(np.all(gap < 0)), margin[i, j],
+                                                 None if forced is None else forced[i, j])
+                if skip:
                     continue                                     # skip block (j, i)
             retained[i, j] = True
             p = np.where(valid, np.exp(st - lse[rows][None, :]), 0.0)
@@ -291,7 +333,7 @@ def mala_backward(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, tiles=No
             dv[cols] += p @ do[rows]
             dk[cols] += scale * (ds @ q[rows])
             dq[rows] += scale * (ds.T @ k[cols])
-    return MalaBackward(dq, dk, dv, retained, legal, margin)
+    return MalaBackward(dq, dk, dv, retained, legal, margin, overridden)
 
 
 # ---------------------------------------------------------------------------
@@ -333,9 +375,10 @@ class MalaDecode:
     retained: np.ndarray   # [T] bool per key tile
     margin: np.ndarray     # [T]
     summaries: list        # per split: (m [G], l [G], u [G, d])
+    overridden: np.ndarray = None  # [T] borderline tiles where a forced decision differed (replay only)
 
 
-def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
+def mala_decode(qg, kc, vc, scale, tau, bk, num_splits, forced=None):
     """One query position of G query heads sharing one KV head, against an
     N-token cache (the cache already holds the current token, so L = N).
 
@@ -345,6 +388,8 @@ def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
     tile; a tile is skipped iff rowmax - m - log l < log(tau / N) holds for
     all G rows (Eq. 3 with the group of heads as the query block, l = 0 =>
     retain).  The splits' (m, l, u) are merged with the exact identity.
+    ``forced`` ([T] bool) replays given decisions at borderline tiles, as in
+    ``mala_forward`` (each split's later tests read the state they produce).
     """
     qg, kc, vc = _f64(qg), _f64(kc), _f64(vc)
     if tau < 0 or not np.isfinite(tau):
@@ -355,6 +400,7 @@ def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
     thr = math.log(tau) - math.log(n) if tau > 0 else None
     retained = np.zeros(t, dtype=bool)
     margin = np.full(t, np.nan)
+    overridden = np.zeros(t, dtype=bool)
     summaries = []
     for sp in range(num_splits):
         m = np.full(g, -np.inf)
@@ -369,7 +415,9 @@ def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
                     ratio = np.where(l > 0, mt - m - np.log(np.where(l > 0, l, 1.0)), np.inf)
                 gap = ratio - thr
                 margin[j] = gap.max()
-                if np.all(gap < 0):
+                skip, overridden[j] = _follow(bool(np.all(gap < 0)), margin[j],
+                                              None if forced is None else forced[j])
+                if skip:
                     continue
             retained[j] = True
             m_new = np.maximum(m, mt)
@@ -387,7 +435,7 @@ def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
         mr, lr, ur = merge_summaries([(m[r], l[r], u[r]) for (m, l, u) in summaries])
         o[r] = ur / lr
         lse[r] = mr + math.log(lr)
-    return MalaDecode(o, lse, retained, margin, summaries)
+    return MalaDecode(o, lse, retained, margin, summaries, overridden)
 
 
 # ---------------------------------------------------------------------------
@@ -396,9 +444,10 @@ def mala_decode(qg, kc, vc, scale, tau, bk, num_splits):
 # ---------------------------------------------------------------------------
 
 def mala_forward_bshd(q, k, v, scale, tau, bq, bk, causal=True, heads=None,
-                      batches=None, query_blocks=None):
+                      batches=None, query_blocks=None, forced=None):
     """q [B, L, Hq, d], k/v [B, L, Hkv, d] -> dict of o [B, L, Hq, d],
-    lse [B, Hq, L], retained/legal/margin [B, Hq, Tr, Tc]."""
+    lse [B, Hq, L], retained/legal/margin/overridden [B, Hq, Tr, Tc].
+    ``forced`` [B, Hq, Tr, Tc]: decisions to replay at borderline tiles."""
     bsz, nq, hq, d = q.shape
     nk, hkv = k.shape[1], k.shape[2]
     grp = hq // hkv
@@ -409,22 +458,25 @@ def mala_forward_bshd(q, k, v, scale, tau, bq, bk, causal=True, heads=None,
         "retained": np.zeros((bsz, hq, tr, tc), dtype=bool),
         "legal": np.zeros((bsz, hq, tr, tc), dtype=bool),
         "margin": np.full((bsz, hq, tr, tc), np.nan),
+        "overridden": np.zeros((bsz, hq, tr, tc), dtype=bool),
     }
     for b in (range(bsz) if batches is None else batches):
         for h in (range(hq) if heads is None else heads):
             r = mala_forward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], scale, tau,
-                             bq, bk, causal, query_blocks)
+                             bq, bk, causal, query_blocks, None if forced is None else forced[b, h])
             out["o"][b, :, h] = r.o
             out["lse"][b, h] = r.lse
             out["retained"][b, h] = r.retained
             out["legal"][b, h] = r.legal
             out["margin"][b, h] = r.margin
+            out["overridden"][b, h] = r.overridden
     return out
 
 
 def mala_backward_bshd(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, heads=None,
-                       batches=None, tiles=None):
-    """Gradients for BSHD inputs; dk/dv of a KV head sum over its query heads."""
+                       batches=None, tiles=None, forced=None):
+    """Gradients for BSHD inputs; dk/dv of a KV head sum over its query heads.
+    ``forced`` [B, Hq, Tr, Tc]: decisions to replay at borderline tiles."""
     bsz, nq, hq, d = q.shape
     nk, hkv = k.shape[1], k.shape[2]
     grp = hq // hkv
@@ -434,27 +486,32 @@ def mala_backward_bshd(q, k, v, o, do, lse, scale, tau, bq, bk, causal=True, hea
         "retained": np.zeros((bsz, hq, tr, tc), dtype=bool),
         "legal": np.zeros((bsz, hq, tr, tc), dtype=bool),
         "margin": np.full((bsz, hq, tr, tc), np.nan),
+        "overridden": np.zeros((bsz, hq, tr, tc), dtype=bool),
     }
     for b in (range(bsz) if batches is None else batches):
         for h in (range(hq) if heads is None else heads):
             r = mala_backward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], o[b, :, h],
-                              do[b, :, h], lse[b, h], scale, tau, bq, bk, causal, tiles)
+                              do[b, :, h], lse[b, h], scale, tau, bq, bk, causal, tiles,
+                              None if forced is None else forced[b, h])
             out["dq"][b, :, h] = r.dq
             out["dk"][b, :, h // grp] += r.dk
             out["dv"][b, :, h // grp] += r.dv
             out["retained"][b, h] = r.retained
             out["legal"][b, h] = r.legal
             out["margin"][b, h] = r.margin
+            out["overridden"][b, h] = r.overridden
     return out
 
 
-def mala_forward_varlen(q, k, v, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None):
+def mala_forward_varlen(q, k, v, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None,
+                        forced=None):
     """Packed variable-length forward: sequence b is rows cu_seqlens[b] ..
     cu_seqlens[b + 1] - 1 of q [total, Hq, d], k / v [total, Hkv, d] and is
     its own context (§2.1 counts L_q per row within it), i.e. exactly
     ``mala_forward_bshd`` on that slice.  Returns o [total, Hq, d], lse
     [Hq, total] and retained / legal / margin [B, Hq, Tm, Tm] with
-    Tm = ceil(max length / bq) (entries past a sequence's tiles False / NaN)."""
+    Tm = ceil(max length / bq) (entries past a sequence's tiles False / NaN).
+    ``forced`` [B, Hq, Tm, Tm]: decisions to replay at borderline tiles."""
     total, hq, d = q.shape
     nseq = len(cu_seqlens) - 1
     lens = [int(cu_seqlens[b + 1]) - int(cu_seqlens[b]) for b in range(nseq)]
@@ -465,22 +522,25 @@ def mala_forward_varlen(q, k, v, cu_seqlens, scale, tau, bq, bk, causal=True, he
         "retained": np.zeros((nseq, hq, tm, tm), dtype=bool),
         "legal": np.zeros((nseq, hq, tm, tm), dtype=bool),
         "margin": np.full((nseq, hq, tm, tm), np.nan),
+        "overridden": np.zeros((nseq, hq, tm, tm), dtype=bool),
     }
     for b in (range(nseq) if seqs is None else seqs):
         s0, n = int(cu_seqlens[b]), lens[b]
         if n == 0:
             continue
-        r = mala_forward_bshd(q[None, s0:s0 + n], k[None, s0:s0 + n], v[None, s0:s0 + n], scale, tau, bq, bk,
-                              causal, heads=heads)
         t = -(-n // bq)
+        fb = None if forced is None else np.asarray(forced)[b:b + 1, :, :t, :t]
+        r = mala_forward_bshd(q[None, s0:s0 + n], k[None, s0:s0 + n], v[None, s0:s0 + n], scale, tau, bq, bk,
+                              causal, heads=heads, forced=fb)
         out["o"][s0:s0 + n] = r["o"][0]
         out["lse"][:, s0:s0 + n] = r["lse"][0]
-        for key in ("retained", "legal", "margin"):
+        for key in ("retained", "legal", "margin", "overridden"):
             out[key][b, :, :t, :t] = r[key][0]
     return out
 
 
-def mala_backward_varlen(q, k, v, o, do, lse, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None):
+def mala_backward_varlen(q, k, v, o, do, lse, cu_seqlens, scale, tau, bq, bk, causal=True, heads=None, seqs=None,
+                         forced=None):
     """Packed variable-length backward (layouts as ``mala_forward_varlen``):
     ``mala_backward_bshd`` on each sequence's slice."""
     total, hq, d = q.shape
@@ -490,26 +550,29 @@ def mala_backward_varlen(q, k, v, o, do, lse, cu_seqlens, scale, tau, bq, bk, ca
     out = {"dq": np.zeros(q.shape), "dk": np.zeros(k.shape), "dv": np.zeros(v.shape),
            "retained": np.zeros((nseq, hq, tm, tm), dtype=bool),
            "legal": np.zeros((nseq, hq, tm, tm), dtype=bool),
-           "margin": np.full((nseq, hq, tm, tm), np.nan)}
+           "margin": np.full((nseq, hq, tm, tm), np.nan),
+           "overridden": np.zeros((nseq, hq, tm, tm), dtype=bool)}
     for b in (range(nseq) if seqs is None else seqs):
         s0, n = int(cu_seqlens[b]), lens[b]
         if n == 0:
             continue
         sl = slice(s0, s0 + n)
-        r = mala_backward_bshd(q[None, sl], k[None, sl], v[None, sl], o[None, sl], do[None, sl],
-                               lse[None, :, sl], scale, tau, bq, bk, causal, heads=heads)
         t = -(-n // bq)
+        fb = None if forced is None else np.asarray(forced)[b:b + 1, :, :t, :t]
+        r = mala_backward_bshd(q[None, sl], k[None, sl], v[None, sl], o[None, sl], do[None, sl],
+                               lse[None, :, sl], scale, tau, bq, bk, causal, heads=heads, forced=fb)
         out["dq"][sl] = r["dq"][0]
         out["dk"][sl] = r["dk"][0]
         out["dv"][sl] = r["dv"][0]
-        for key in ("retained", "legal", "margin"):
+        for key in ("retained", "legal", "margin", "overridden"):
             out[key][b, :, :t, :t] = r[key][0]
     return out
 
 
-def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None):
+def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None, forced=None):
     """q [B, Hq, d], caches [B, N, Hkv, d] -> o [B, Hq, d], lse [B, Hq],
-    retained/margin [B, Hkv, T]."""
+    retained/margin/overridden [B, Hkv, T].  ``forced`` [B, Hkv, T]:
+    decisions to replay at borderline tiles."""
     bsz, hq, d = q.shape
     n, hkv = k_cache.shape[1], k_cache.shape[2]
     grp = hq // hkv
@@ -518,22 +581,25 @@ def mala_decode_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=Non
     lse = np.full((bsz, hq), np.nan)
     retained = np.zeros((bsz, hkv, t), dtype=bool)
     margin = np.full((bsz, hkv, t), np.nan)
+    overridden = np.zeros((bsz, hkv, t), dtype=bool)
     for b in (range(bsz) if batches is None else batches):
         for hk in range(hkv):
             r = mala_decode(q[b, hk * grp:(hk + 1) * grp], k_cache[b, :, hk], v_cache[b, :, hk],
-                            scale, tau, bk, num_splits)
+                            scale, tau, bk, num_splits, None if forced is None else forced[b, hk])
             o[b, hk * grp:(hk + 1) * grp] = r.o
             lse[b, hk * grp:(hk + 1) * grp] = r.lse
             retained[b, hk] = r.retained
             margin[b, hk] = r.margin
-    return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+            overridden[b, hk] = r.overridden
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin, "overridden": overridden}
 
 
-def mala_decode_per_head_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None):
+def mala_decode_per_head_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, batches=None, forced=None):
     """Per-head decode: the skip rule of §2.2 with each query head as its own
     one-row query block, i.e. ``mala_decode`` on each head alone against its
     KV head (same splits, order and merge).  q [B, Hq, d], caches
-    [B, N, Hkv, d] -> o [B, Hq, d], lse [B, Hq], retained/margin [B, Hq, T]."""
+    [B, N, Hkv, d] -> o [B, Hq, d], lse [B, Hq], retained/margin/overridden
+    [B, Hq, T].  ``forced`` [B, Hq, T]: decisions to replay at borderline tiles."""
     bsz, hq, d = q.shape
     n, hkv = k_cache.shape[1], k_cache.shape[2]
     grp = hq // hkv
@@ -542,24 +608,29 @@ def mala_decode_per_head_bhd(q, k_cache, v_cache, scale, tau, bk, num_splits, ba
     lse = np.full((bsz, hq), np.nan)
     retained = np.zeros((bsz, hq, t), dtype=bool)
     margin = np.full((bsz, hq, t), np.nan)
+    overridden = np.zeros((bsz, hq, t), dtype=bool)
     for b in (range(bsz) if batches is None else batches):
         for h in range(hq):
             r = mala_decode(q[b, h:h + 1], k_cache[b, :, h // grp], v_cache[b, :, h // grp],
-                            scale, tau, bk, num_splits)
+                            scale, tau, bk, num_splits, None if forced is None else forced[b, h])
             o[b, h] = r.o[0]
             lse[b, h] = r.lse[0]
             retained[b, h] = r.retained
             margin[b, h] = r.margin
-    return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+            overridden[b, h] = r.overridden
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin, "overridden": overridden}
 
 
-def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_splits, batches=None):
+def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_splits, batches=None,
+                           forced=None):
     """Variable-length decode: sequence b attends to the first cache_lens[b]
     rows of its (padded) cache, which hold its current token, so its L is
     cache_lens[b] (§2.1: L counts the query's own causal context; App. A.1
     for the split-KV decode).  Each sequence is exactly ``mala_decode`` on its
-    truncated cache.  retained / margin are [B, Hkv, ceil(N_max / bk)], with
-    tiles past a sequence's own tiles left False / NaN."""
+    truncated cache.  retained / margin / overridden are
+    [B, Hkv, ceil(N_max / bk)], with tiles past a sequence's own tiles left
+    False / NaN.  ``forced`` (same shape): decisions to replay at borderline
+    tiles."""
     bsz, hq, d = q.shape
     n_max, hkv = k_cache.shape[1], k_cache.shape[2]
     grp = hq // hkv
@@ -568,6 +639,7 @@ def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_
     lse = np.full((bsz, hq), np.nan)
     retained = np.zeros((bsz, hkv, t_max), dtype=bool)
     margin = np.full((bsz, hkv, t_max), np.nan)
+    overridden = np.zeros((bsz, hkv, t_max), dtype=bool)
     for b in (range(bsz) if batches is None else batches):
         n = int(cache_lens[b])
         if not 1 <= n <= n_max:
@@ -575,12 +647,13 @@ def mala_decode_varlen_bhd(q, k_cache, v_cache, cache_lens, scale, tau, bk, num_
         t = -(-n // bk)
         for hk in range(hkv):
             r = mala_decode(q[b, hk * grp:(hk + 1) * grp], k_cache[b, :n, hk], v_cache[b, :n, hk],
-                            scale, tau, bk, num_splits)
+                            scale, tau, bk, num_splits, None if forced is None else np.asarray(forced)[b, hk, :t])
             o[b, hk * grp:(hk + 1) * grp] = r.o
             lse[b, hk * grp:(hk + 1) * grp] = r.lse
             retained[b, hk, :t] = r.retained
             margin[b, hk, :t] = r.margin
-    return {"o": o, "lse": lse, "retained": retained, "margin": margin}
+            overridden[b, hk, :t] = r.overridden
+    return {"o": o, "lse": lse, "retained": retained, "margin": margin, "overridden": overridden}
 
 
 # ---------------------------------------------------------------------------
@@ -601,8 +674,8 @@ def legal_tiles(n_q, n_k, bq, bk, causal=True):
 
 
 def tile_reference_mass(q, k, scale, bq, bk, causal=True):
-    """Reference mass of every region (App. C.2: the screening-disabled
-    reference "provides the probability mass of every candidate region"): the
+    """Reference mass of every region (App. C.2: the operator with screening
+    disabled serves as the reference mass of each candidate region): the
     dense softmax probabilities of tile j's keys summed over the rows of query
     block i.  Returns [Tr, Tc]; illegal tiles have mass 0, and each block's
     masses add up to its number of rows."""

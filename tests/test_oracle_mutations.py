@@ -20,8 +20,8 @@ MUTATIONS = [
      "mt - m + np.log(np.where(l > 0, l, 1.0)), np.inf)\n                gap = (ratio - thr)[has]"),
     ("L_q off by one", "return np.arange(1, n_q + 1, dtype=np.float64)",
      "return np.arange(2, n_q + 2, dtype=np.float64)"),
-    ("any instead of all", "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                if np.all(gap < 0):",
-     "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                if np.any(gap < 0):"),
+    ("any instead of all", "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                skip, overridden[i, j] = _follow(bool(np.all(gap < 0))",
+     "gap = (ratio - thr)[has]\n                margin[i, j] = gap.max()\n                skip, overridden[i, j] = _follow(bool(np.any(gap < 0))"),
     ("decode L off by one", "thr = math.log(tau) - math.log(n) if tau > 0 else None",
      "thr = math.log(tau) - math.log(n + 1) if tau > 0 else None"),
     ("ascending forward traversal", "for j in reversed(range(tc)):", "for j in range(tc):"),
@@ -46,6 +46,10 @@ MUTATIONS = [
     ("selection keeps lowest mass", "key=lambda j: (-mass[i, j], -j))", "key=lambda j: (mass[i, j], -j))"),
     ("rounding extra by value", "out[i, h, qb] = base + (1 if (i - cell) % n < extra else 0)",
      "out[i, h, qb] = base + (1 if counts[i, h, qb] > base else 0)"),
+    ("replay follows every tile", "if forced is None or not is_borderline(margin):", "if forced is None:"),
+    ("replay ignores the forced mask", "if forced is None or not is_borderline(margin):", "if True:"),
+    ("replay band on the log margin", "return np.isfinite(m) & (np.abs(np.expm1(m)) <= BORDERLINE_REL)",
+     "return np.isfinite(m) & (np.abs(m) <= 0.25)"),
     ("position pools one head", "total = int(sum(counts[i, h, qb] for i in range(n_in) for h in range(n_h)))",
      "total = int(sum(counts[i, 0, qb] for i in range(n_in) for h in range(n_h)))"),
 ]
@@ -72,6 +76,11 @@ PIN_TESTS = [
     (pins.test_matched_work_allocation_closed_form, {}),
     (pins.test_matched_work_allocation_matches_work_exactly, {"scope": "head_position"}),
     (pins.test_matched_work_allocation_matches_work_exactly, {"scope": "position"}),
+    (pins.test_replay_follows_a_borderline_tile_and_the_later_tests_follow_the_state, {}),
+    (pins.test_replay_ignores_forced_decisions_at_tiles_that_are_not_borderline, {}),
+    (pins.test_replay_with_the_runs_own_decisions_or_their_complement_is_the_run, {}),
+    (pins.test_decode_replay_closed_form, {}),
+    (pins.test_backward_replay_follows_only_borderline_tiles, {}),
 ]
 
 

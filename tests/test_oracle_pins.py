@@ -674,3 +674,102 @@ def test_matched_work_allocation_matches_work_exactly(scope):
     np.testing.assert_array_equal(alloc.sum(axis=axes), counts.sum(axis=axes))    # per cell, so in total
     assert (alloc.max(axis=axes) - alloc.min(axis=axes) <= 1).all()              # one allocation per cell
     assert (alloc >= 1).all() and (alloc <= legal_per_block).all()
+
+
+# ---------------------------------------------------------------------------
+# Forced-decision replay (MALA §2.2 Eq. 3 and Algorithm 1: each test reads the
+# (m, l) that the earlier decisions produced), used by the parity checks at
+# borderline tiles.
+# ---------------------------------------------------------------------------
+
+def three_key_case():
+    """Causal rows 0-2 with d = 1, scale 1 and one-key tiles, so row 2 visits
+    keys 2, 1, 0 (newest first) with scores 0, log 0.5, log 0.6; tau = 1.5, so
+    row 2's threshold is tau / L = 0.5 on the ratio exp(s) / Z.  Key 2 is kept
+    (l = 0).  Key 1's ratio is 0.5 / 1: exactly the threshold, a borderline
+    tile.  Key 0's ratio is 0.6 / 1.5 = 0.4 (skip) if key 1 was kept and
+    0.6 / 1 = 0.6 (keep) if it was not: both 20% from the threshold."""
+    q = np.ones((3, 1))
+    k = np.array([[math.log(0.6)], [math.log(0.5)], [0.0]])
+    v = np.array([[1.0], [10.0], [100.0]])
+    return q, k, v, 1.5
+
+
+def test_replay_follows_a_borderline_tile_and_the_later_tests_follow_the_state():
+    q, k, v, tau = three_key_case()
+    free = orc.mala_forward(q, k, v, 1.0, tau, 1, 1)
+    assert orc.is_borderline(free.margin[2, 1])
+    # kept key 1: Z = 1.5, key 0 skipped; o = (0.5 * 10 + 100) / 1.5
+    r = orc.mala_forward(q, k, v, 1.0, tau, 1, 1, forced=np.tril(np.ones((3, 3), bool)))
+    assert r.retained[2].tolist() == [False, True, True]
+    assert r.o[2, 0] == pytest.approx(105.0 / 1.5, rel=1e-14)
+    assert r.lse[2] == pytest.approx(math.log(1.5), rel=1e-14)
+    assert r.margin[2, 0] == pytest.approx(math.log(0.8), rel=1e-12)
+    # skipped key 1: Z = 1, key 0 kept; o = (0.6 * 1 + 100) / 1.6
+    forced = np.tril(np.ones((3, 3), bool))
+    forced[2, 1] = False
+    r = orc.mala_forward(q, k, v, 1.0, tau, 1, 1, forced=forced)
+    assert r.retained[2].tolist() == [True, False, True]
+    assert r.o[2, 0] == pytest.approx(100.6 / 1.6, rel=1e-14)
+    assert r.lse[2] == pytest.approx(math.log(1.6), rel=1e-14)
+    assert r.margin[2, 0] == pytest.approx(math.log(1.2), rel=1e-12)
+    # rows 0 and 1 have no borderline tile and are untouched by the forced mask
+    for rr in (0, 1):
+        assert r.retained[rr].tolist() == free.retained[rr].tolist()
+        assert r.o[rr, 0] == free.o[rr, 0]
+
+
+def test_replay_ignores_forced_decisions_at_tiles_that_are_not_borderline():
+    q, k, v, tau = three_key_case()
+    # key 0 of row 2 is 20% from the threshold on either path: never followed
+    forced = np.zeros((3, 3), bool)
+    forced[2, 2] = True                        # key 1 skipped, and key 0 "skipped" (ignored)
+    r = orc.mala_forward(q, k, v, 1.0, tau, 1, 1, forced=forced)
+    assert r.retained[2].tolist() == [True, False, True]
+    assert r.retained[1].tolist() == [True, True, False]      # row 1 keeps both keys regardless
+    forced = np.ones((3, 3), bool)             # key 1 kept, and key 0 "kept" (ignored)
+    r = orc.mala_forward(q, k, v, 1.0, tau, 1, 1, forced=forced)
+    assert r.retained[2].tolist() == [False, True, True]
+
+
+def test_replay_with_the_runs_own_decisions_or_their_complement_is_the_run():
+    """On inputs with no borderline tile any forced mask leaves every result
+    unchanged; with the run's own mask nothing is overridden."""
+    q, k, v, _ = _peaked(L=192, seed=21)
+    free = orc.mala_forward(q, k, v, PIN_SCALE, 1.0, 16, 16)
+    assert not orc.is_borderline(free.margin).any()
+    assert (~free.retained & free.legal).any() and free.retained.any()
+    for forced in (free.retained, ~free.retained):
+        r = orc.mala_forward(q, k, v, PIN_SCALE, 1.0, 16, 16, forced=forced)
+        for name in ("o", "lse", "retained", "legal", "margin"):
+            np.testing.assert_array_equal(getattr(r, name), getattr(free, name))
+        assert not r.overridden.any()
+
+
+def test_decode_replay_closed_form():
+    """The three keys as a one-query cache (N = 3, one split): the same path
+    dependence as row 2 of the prefill case."""
+    _, k, v, tau = three_key_case()
+    qg = np.ones((1, 1))
+    free = orc.mala_decode(qg, k, v, 1.0, tau, 1, 1)
+    assert orc.is_borderline(free.margin[1])
+    r = orc.mala_decode(qg, k, v, 1.0, tau, 1, 1, forced=np.array([False, False, True]))
+    assert r.retained.tolist() == [True, False, True]
+    assert r.o[0, 0] == pytest.approx(100.6 / 1.6, rel=1e-14)
+    r = orc.mala_decode(qg, k, v, 1.0, tau, 1, 1, forced=np.array([True, True, True]))
+    assert r.retained.tolist() == [False, True, True]
+    assert r.lse[0] == pytest.approx(math.log(1.5), rel=1e-14)
+
+
+def test_backward_replay_follows_only_borderline_tiles():
+    """One query, one key, S = 0, tau = 1, L = 1: the Eq. 4 margin S - lse is
+    exactly 0 at lse = 0 (borderline) and 1 at lse = -1 (kept, P = e)."""
+    q = k = v = do = o = np.ones((1, 1))
+    k = np.zeros((1, 1))
+    for forced, dv in ((True, 1.0), (False, 0.0)):
+        r = orc.mala_backward(q, k, v, o, do, np.zeros(1), 1.0, 1.0, 1, 1, forced=np.array([[forced]]))
+        assert r.retained[0, 0] == forced
+        assert r.dv[0, 0] == pytest.approx(dv, abs=1e-15)
+    r = orc.mala_backward(q, k, v, o, do, np.array([-1.0]), 1.0, 1.0, 1, 1, forced=np.array([[False]]))
+    assert r.retained[0, 0]
+    assert r.dv[0, 0] == pytest.approx(math.e, rel=1e-14)
