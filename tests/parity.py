@@ -10,13 +10,15 @@ Tolerances (written here once and used by every parity test):
                    ratio lies within 1e-3 (relative) of tau / L_q may be decided
                    either way.
 
-A flipped borderline forward tile changes the online state of its query block,
-so every later decision and the block's output may differ; such blocks are
-left out of the element-wise comparison and checked instead for validity: the
-GPU output must equal softmax renormalised over the tiles the GPU kept, and
-the first disagreement in traversal order must be borderline.  Backward tiles
-are decided independently; a flipped borderline tile excludes the rows it
-touches.
+A borderline forward tile decided the other way changes the online state of
+its query block, so later decisions and the block's output may change with
+it.  Such a block is replayed: the oracle runs it again, following the GPU's
+decision at each tile that is borderline on the replay's own state and
+deciding every other tile itself.  Every GPU decision must then equal the
+replay's, bit for bit, and the block's outputs are compared with the replay's
+element by element.  Decode rows are replayed the same way; backward tiles
+are decided independently, and a backward replay follows the GPU at its
+borderline tiles only.  No row is left out of the comparison.
 """
 from __future__ import annotations
 
@@ -44,9 +46,7 @@ def round_like(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
 
 
 def is_borderline(margin) -> np.ndarray:
-    m = np.asarray(margin, dtype=np.float64)
-    with np.errstate(over="ignore", invalid="ignore"):
-        return np.isfinite(m) & (np.abs(np.expm1(m)) <= orc.BORDERLINE_REL)
+    return orc.is_borderline(margin)
 
 
 FP16_UNIT_ROUNDOFF = 2.0 ** -11
@@ -101,68 +101,89 @@ def check_close_bf16_rounded(name, got, ref):
     return {"max_abs": float(err.max()), "mean_rel": mean_rel}
 
 
-def fwd_block_agreement(gpu_mask, ref_retained, ref_legal, ref_margin):
-    """Per query block: True if every legal decision agrees.  Asserts that any
-    block that disagrees does so first (in the diagonal-to-oldest traversal)
-    at a borderline tile.  Arrays are [Tr, Tc] for one (b, h)."""
-    tr = ref_legal.shape[0]
-    agree = np.ones(tr, dtype=bool)
-    for i in range(tr):
-        legal = ref_legal[i]
-        if not legal.any():
-            continue
-        diff = (gpu_mask[i].astype(bool) != ref_retained[i]) & legal
-        if diff.any():
-            agree[i] = False
-            first = np.nonzero(diff)[0].max()            # traversal runs from high j to low j
-            assert is_borderline(ref_margin[i, first]), \
-                f"query block {i}: tile {first} decided differently with margin {ref_margin[i, first]:.4g}"
-    return agree
-
-
-def check_forward(gpu_o, gpu_lse, gpu_mask, ref, q, k, v, scale, block, out_dtype, fp32,
+def check_forward(gpu_o, gpu_lse, gpu_mask, ref, q, k, v, scale, tau, block, out_dtype, fp32,
                   heads, causal=True, blocks=None):
     """Compare forward results (numpy: o BSHD, lse [B,H,L], mask [B,H,Tr,Tc])
     with the oracle dict from mala_forward_bshd on the listed query ``heads``;
-    ``blocks`` restricts the comparison to those query blocks.  Returns metrics."""
+    ``blocks`` restricts the comparison to those query blocks.
+
+    A query block whose GPU decisions differ from the oracle's anywhere is
+    replayed: the oracle runs the block again following the GPU's decision at
+    each tile that is borderline on the replay's own (m, l), and deciding every
+    other tile itself (``forced``).  Every GPU decision must then equal the
+    replay's, and the block's O and lse are compared with the replay's.  So
+    every decision and every row is checked; a borderline tile only chooses
+    which of the two valid paths the expected values follow.  Returns metrics."""
     B, L, H, D = gpu_o.shape
     grp = H // k.shape[2]
     tr = ref["legal"].shape[2]
     blocks = list(range(tr)) if blocks is None else list(blocks)
+    exp_o = np.array(ref["o"], dtype=np.float64, copy=True)
+    exp_lse = np.array(ref["lse"], dtype=np.float64, copy=True)
     rows_ok = np.zeros((B, H, L), dtype=bool)
-    flipped = 0
+    replayed = overridden = 0
     for b in range(B):
         for h in heads:
-            agree = fwd_block_agreement(gpu_mask[b, h], ref["retained"][b, h], ref["legal"][b, h],
-                                        ref["margin"][b, h])
+            legal = ref["legal"][b, h]
+            g = gpu_mask[b, h].astype(bool)
+            diff = [i for i in blocks if ((g[i] != ref["retained"][b, h, i]) & legal[i]).any()]
+            if diff:
+                rep = orc.mala_forward(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp], scale, tau, block, block,
+                                       causal, query_blocks=diff, forced=g)
+                for i in diff:
+                    bad = (g[i] != rep.retained[i]) & rep.legal[i]
+                    assert not bad.any(), (
+                        f"(b={b}, h={h}) query block {i}: tiles {np.flatnonzero(bad).tolist()} decided differently "
+                        f"from the oracle's replay of the GPU's borderline decisions; margins {rep.margin[i, bad]}")
+                    r0, r1 = i * block, min(L, (i + 1) * block)
+                    exp_o[b, r0:r1, h] = rep.o[r0:r1]
+                    exp_lse[b, h, r0:r1] = rep.lse[r0:r1]
+                replayed += len(diff)
+                overridden += int(rep.overridden.sum())
             for i in blocks:
-                r0, r1 = i * block, min(L, (i + 1) * block)
-                if agree[i]:
-                    rows_ok[b, h, r0:r1] = True
-                    continue
-                flipped += 1
-                keep = gpu_mask[b, h].astype(bool) & ref["legal"][b, h]
-                rows = np.arange(r0, r1)
-                o_r, lse_r = orc.restricted_attention(q[b, :, h], k[b, :, h // grp], v[b, :, h // grp],
-                                                      scale, keep, block, block, causal, rows)
-                check_close("o (flipped block)", gpu_o[b, r0:r1, h], o_r, out_dtype, fp32=fp32)
-                assert np.abs(gpu_lse[b, h, r0:r1] - lse_r).max() <= LSE_ABS
+                rows_ok[b, h, i * block:min(L, (i + 1) * block)] = True
     n_blocks = B * len(heads) * len(blocks)
-    assert flipped <= max(1, MAX_FLIPPED_FRACTION * n_blocks), f"{flipped} of {n_blocks} blocks flipped"
+    assert replayed <= max(1, MAX_FLIPPED_FRACTION * n_blocks), f"{replayed} of {n_blocks} blocks replayed"
     sel = np.transpose(rows_ok, (0, 2, 1))               # [B, L, H]
-    metrics = check_close("o", gpu_o[sel], ref["o"][sel], out_dtype, fp32=fp32)
-    lse_err = np.abs(gpu_lse[rows_ok] - ref["lse"][rows_ok]).max()
+    metrics = check_close("o", gpu_o[sel], exp_o[sel], out_dtype, fp32=fp32)
+    lse_err = np.abs(gpu_lse[rows_ok] - exp_lse[rows_ok]).max()
     assert lse_err <= LSE_ABS, f"lse max abs err {lse_err:.3g}"
     legal = ref["legal"][:, heads][:, :, blocks]
-    metrics.update(lse_max_abs=float(lse_err), flipped_blocks=flipped,
+    metrics.update(lse_max_abs=float(lse_err), replayed_blocks=replayed, overridden_tiles=overridden,
                    kept=int(ref["retained"][:, heads][:, :, blocks].sum()), legal=int(legal.sum()))
     return metrics
 
 
-def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=True, grad_dtype=torch.float32):
+def decode_expected(gpu_mask, ref_o, ref_lse, ref_retained, q, k, v, scale, tau, block, splits):
+    """Expected results of one decision row of a decode (a KV head's group of
+    query heads, or one query head): ref_o [G, d], ref_lse [G], masks [T];
+    q [G, d] and the cache k, v [N, d] it attends to.  If the GPU's tile
+    decisions differ from the oracle's, the row is replayed with the GPU's
+    decisions at borderline tiles (``mala_decode(..., forced=...)``) and every
+    decision must equal the replay's; the replay's O and lse are then the
+    expected values.  Returns (o, lse, replayed)."""
+    g = np.asarray(gpu_mask, bool)
+    if not (g != np.asarray(ref_retained, bool)).any():
+        return ref_o, ref_lse, False
+    rep = orc.mala_decode(q, k, v, scale, tau, block, splits, forced=g)
+    bad = g != rep.retained
+    assert not bad.any(), (f"decode tiles {np.flatnonzero(bad).tolist()} decided differently from the oracle's "
+                           f"replay of the GPU's borderline decisions; margins {rep.margin[bad]}")
+    return rep.o, rep.lse, True
+
+
+def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=True, grad_dtype=torch.float32,
+                   replay=None):
     """gpu / ref: dicts with dq, dk, dv (numpy, BSHD) and mask / retained,
     legal, margin ([B, H, Tr, Tc]).  ``dq_rows`` / ``dk_rows`` restrict the
     comparison to boolean masks [B, L, H] / [B, L, Hkv] (sampled checks).
+
+    Backward decisions read only the fixed lse (Eq. 4), so they are
+    independent.  If the GPU decided any tile differently, ``replay()`` must
+    return the oracle's backward run again with ``forced`` = the GPU's mask
+    (the same dict layout): it follows the GPU exactly at the tiles that are
+    borderline for it.  Every GPU decision must then equal the replay's, and
+    all gradients are compared with the replay's.
 
     With grouped query heads, dK and dV sum over the group, so they grow with
     it while their error stays near fp16's unit roundoff relative to the
@@ -173,17 +194,19 @@ def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=Tru
     grp = H // Hkv
     okq = np.ones((B, Lq, H), bool) if dq_rows is None else dq_rows.copy()
     okk = np.ones((B, Lk, Hkv), bool) if dk_rows is None else dk_rows.copy()
-    legal = ref["legal"]
-    diff = (gpu["mask"].astype(bool) != ref["retained"]) & legal
+    gmask = gpu["mask"].astype(bool)
+    diff = (gmask != ref["retained"]) & ref["legal"]
+    metrics = {"replayed_tiles": int(diff.sum())}
     if diff.any():
-        bs, hs, iis, jjs = np.nonzero(diff)
-        for b, h, i, j in zip(bs, hs, iis, jjs):
-            assert is_borderline(ref["margin"][b, h, i, j]), \
-                f"bwd tile (b={b}, h={h}, i={i}, j={j}) decided differently, margin {ref['margin'][b, h, i, j]:.4g}"
-            okq[b, i * block:(i + 1) * block, h] = False
-            okk[b, j * block:(j + 1) * block, h // grp] = False
-    assert diff.sum() <= max(1, MAX_FLIPPED_FRACTION * legal.sum())
-    metrics = {"flipped_tiles": int(diff.sum())}
+        assert replay is not None, "the GPU decided backward tiles differently and no replay was given"
+        assert diff.sum() <= max(1, MAX_FLIPPED_FRACTION * ref["legal"].sum())
+        ref = replay()
+        bad = (gmask != ref["retained"]) & ref["legal"]
+        if bad.any():
+            b, h, i, j = (int(x[0]) for x in np.nonzero(bad))
+            raise AssertionError(f"{int(bad.sum())} bwd tiles decided differently from the oracle's replay, e.g. "
+                                 f"(b={b}, h={h}, i={i}, j={j}) with margin {ref['margin'][b, h, i, j]:.4g}")
+        metrics["overridden_tiles"] = int(ref["overridden"].sum())
     for name, ok in (("dq", okq), ("dk", okk), ("dv", okk)):
         if grad_dtype == torch.bfloat16:
             metrics[name] = check_close_bf16_rounded(name, gpu[name][ok], ref[name][ok])

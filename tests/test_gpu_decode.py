@@ -46,34 +46,24 @@ def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None
     rows = [(h, slice(h, h + 1), h // grp) for h in range(Hq)] if per_head else \
         [(hk, slice(hk * grp, (hk + 1) * grp), hk) for hk in range(Hkv)]
     fp32 = q.dtype == torch.float32
-    ok = np.zeros((B, Hq), bool)
-    flipped = 0
+    replayed = 0
     counts = info["counts"].cpu().numpy()
+    exp_o, exp_lse = ref["o"].copy(), ref["lse"].copy()
     for b in batches:
         n_b = N if lens is None else lens[b]
         T = -(-n_b // block)
         per = -(-T // splits)
         for row, hs, hk in rows:
-            diff = gmask[b, row, :T].astype(bool) != ref["retained"][b, row, :T]
             for sp in range(splits):
                 np.testing.assert_array_equal(counts[b, row, sp], gmask[b, row, sp * per:min(T, (sp + 1) * per)].sum())
-            if not diff.any():
-                ok[b, hs] = True
-                continue
-            # the first disagreement inside each split (newest tile first) must be borderline
-            for sp in range(splits):
-                idx = [j for j in range(min(T, (sp + 1) * per) - 1, sp * per - 1, -1) if diff[j]]
-                if idx:
-                    assert parity.is_borderline(ref["margin"][b, row, idx[0]])
-            flipped += 1
-            keep = gmask[b, row, :T].astype(bool)[None, :]
-            nrow = hs.stop - hs.start
-            o_r, lse_r = orc.restricted_attention(q64[b, hs], k64[b, :n_b, hk], v64[b, :n_b, hk], scale, keep,
-                                                  nrow, block, causal=False)
-            parity.check_close("o (flipped)", go[b, hs], o_r, q.dtype, fp32=fp32)
-    assert flipped <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * len(rows))
-    m = parity.check_close("o", go[ok], ref["o"][ok], q.dtype, fp32=fp32)
-    assert np.abs(glse[ok] - ref["lse"][ok]).max() <= parity.LSE_ABS
+            # every decision must equal the oracle's, or its replay of the GPU's borderline decisions
+            exp_o[b, hs], exp_lse[b, hs], rep = parity.decode_expected(
+                gmask[b, row, :T], ref["o"][b, hs], ref["lse"][b, hs], ref["retained"][b, row, :T], q64[b, hs],
+                k64[b, :n_b, hk], v64[b, :n_b, hk], scale, tau, block, splits)
+            replayed += rep
+    assert replayed <= max(1, parity.MAX_FLIPPED_FRACTION * len(batches) * len(rows))
+    m = parity.check_close("o", go[batches], exp_o[batches], q.dtype, fp32=fp32)
+    assert np.abs(glse[batches] - exp_lse[batches]).max() <= parity.LSE_ABS
     return m, gmask
 
 

@@ -38,4 +38,4 @@ def test_expired_wait_is_reported_and_the_context_stays_usable():
     scale = 1 / math.sqrt(128)
     ref = orc.mala_forward_bshd(q64, k64, v64, scale, 1.0, 128, 128)
     parity.check_forward(parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy(), ref, q64, k64, v64,
-                         scale, 128, o.dtype, False, heads=[0, 1])
+                         scale, 1.0, 128, o.dtype, False, heads=[0, 1])

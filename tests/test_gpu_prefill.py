@@ -76,7 +76,7 @@ def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, gr
     ref = orc.mala_forward_bshd(q64, k64, v64, scale, tau, block, block, causal=causal, heads=ref_heads,
                                 query_blocks=fwd_blocks)
     gpu_o, gpu_lse, gpu_mask = parity.to64(o), parity.to64(lse), info["mask"].cpu().numpy()
-    metrics = parity.check_forward(gpu_o, gpu_lse, gpu_mask, ref, q64, k64, v64, scale, block, o.dtype,
+    metrics = parity.check_forward(gpu_o, gpu_lse, gpu_mask, ref, q64, k64, v64, scale, tau, block, o.dtype,
                                    fp32, heads=ref_heads, causal=causal, blocks=q_blocks)
     counts = info["counts"].cpu().numpy()
     legal_gpu = np.tril(np.ones((tr, tc), bool)) if causal else np.ones((tr, tc), bool)
@@ -121,8 +121,14 @@ def _run_case(cfg, L, tau, seed, heads=None, hkv=None, block=None, fp32=None, gr
         if h not in ref_heads:
             sel_legal[:, h] = False
     refb_cmp = dict(refb, legal=sel_legal)
+
+    def replay():
+        r = orc.mala_backward_bshd(q64, k64, v64, o_in64, do64, lse_in64, scale, tau, block, block,
+                                   causal=causal, heads=ref_heads, tiles=tiles, forced=gmask.astype(bool))
+        return dict(r, legal=sel_legal)
+
     bm = parity.check_backward(gpu_b, refb_cmp, block, fp32, dq_rows=dq_rows, dk_rows=dk_rows,
-                               grad_dtype=grad_dtype)
+                               grad_dtype=grad_dtype, replay=replay)
     # backward support is nested in the forward support on oracle-fed rows (MALA §2.2)
     assert not (refb["retained"] & ~ref["retained"] & sel_legal).any()
     np.testing.assert_array_equal(binfo["counts"].cpu().numpy(), (gmask.astype(bool) & legal_gpu).sum(-2))
@@ -197,14 +203,49 @@ def test_prefill_8k_full_size():
 
 @pytest.mark.parametrize("tau", [1.0, 0.0])
 def test_prefill_32k_sampled(tau):
+    """All 8 heads at full size; query blocks at both ends and the middle, dQ
+    at both ends, dK / dV of the last two key blocks."""
     cfg = synthetic.CONFIGS["prefill_32k"]
     tr = cfg.L // cfg.block
-    _run_case(cfg, cfg.L, tau, cfg.seed, ref_heads=[1, 6], q_blocks=[0, 1, tr // 2, tr - 1],
-              dq_blocks=[0, 2], dk_blocks=[tr - 2, tr - 1])
+    _run_case(cfg, cfg.L, tau, cfg.seed, ref_heads=list(range(cfg.H)), q_blocks=[0, 1, tr // 2, tr - 2, tr - 1],
+              dq_blocks=[0, 2, tr - 1], dk_blocks=[tr - 2, tr - 1])
 
 
-def test_prefill_128k_sampled():
+def test_prefill_32k_first_key_block_gradients():
+    """dK / dV of key block 0 (every query row of the sequence contributes, so
+    the oracle runs the whole forward of the head to give the backward its O
+    and lse) and dQ of the last query block, on head 0."""
+    cfg = synthetic.CONFIGS["prefill_32k"]
+    tr = cfg.L // cfg.block
+    _run_case(cfg, cfg.L, 1.0, cfg.seed, ref_heads=[0], q_blocks=[tr - 1], dq_blocks=[tr - 1], dk_blocks=[0])
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.0])
+def test_prefill_128k_sampled(tau):
+    """All 8 heads at full size, tau = 1 and the dense tau = 0 that the
+    benchmark times beside it: query blocks {0, 1, 511, 1022, 1023}; dQ of
+    query blocks 1 and 1022; dK / dV of the last two key blocks."""
     cfg = synthetic.CONFIGS["prefill_128k"]
     tr = cfg.L // cfg.block
-    _run_case(cfg, cfg.L, 1.0, cfg.seed, ref_heads=[4], q_blocks=[0, 1, tr - 1],
-              dq_blocks=[1], dk_blocks=[tr - 1])
+    _run_case(cfg, cfg.L, tau, cfg.seed, ref_heads=list(range(cfg.H)), q_blocks=[0, 1, tr // 2 - 1, tr - 2, tr - 1],
+              dq_blocks=[1, tr - 2], dk_blocks=[tr - 2, tr - 1])
+
+
+def test_bf16_input_beyond_fp16_range_is_reported():
+    """The tensor-core backward takes fp16 operands: a finite bf16 input beyond
+    65504 sets bit 4 of the device status word; 65280, the largest bf16 value
+    below it, does not."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    q, k, v, do = _gpu(*_inputs(cfg, L=256, seed=5, heads=2, hkv=2))
+    o, lse, _ = api.forward(q, k, v, 1.0)
+    torch.cuda.synchronize()
+    assert api.mala_device_status() == 0
+    for name, val, want in (("v", 65280.0, 0), ("v", 70000.0, 4), ("do", -1.0e5, 4), ("q", 3.0e38, 4)):
+        args = {"q": q, "k": k, "v": v, "do": do}
+        t = args[name].clone()
+        t[0, 3, 1, 5] = val
+        args[name] = t
+        api.backward(args["q"], args["k"], args["v"], o, args["do"], lse, 1.0)
+        torch.cuda.synchronize()
+        assert api.mala_device_status() == want, (name, val)
+    assert api.mala_device_status() == 0

@@ -4,7 +4,7 @@ batches) against the oracle, through the C ABI.
 Each sequence is drawn by its workload's recipe at its own length and the
 sequences are packed along one token axis.  Every sequence's slice is then
 checked exactly as a one-sequence mala_fwd / mala_bwd call is (element by
-element, borderline tiles handled the same way).  Equal lengths must give
+element, borderline tiles replayed the same way).  Equal lengths must give
 bit-for-bit what the fixed-length batched call gives, and a sequence whose
 bounds break the contract raises the status bit and is left unwritten.
 """
@@ -63,7 +63,7 @@ def _run(cfg, lens, tau, seed, heads=None, hkv=None, grad_dtype=torch.float32, c
         rb["o"] = ref["o"][None, sl]
         rb["lse"] = ref["lse"][None, :, sl]
         parity.check_forward(go[None, sl], glse[None, :, sl], gmask[b:b + 1, :, :t, :t], rb, q64[None, sl],
-                             k64[None, sl], v64[None, sl], scale, block, o.dtype, fp32, heads=list(range(H)),
+                             k64[None, sl], v64[None, sl], scale, tau, block, o.dtype, fp32, heads=list(range(H)),
                              causal=causal)
         legal = np.tril(np.ones((t, t), bool)) if causal else np.ones((t, t), bool)
         np.testing.assert_array_equal(counts[b, :, :t], (gmask[b, :, :t, :t].astype(bool) & legal).sum(-1))
@@ -86,7 +86,14 @@ def _run(cfg, lens, tau, seed, heads=None, hkv=None, grad_dtype=torch.float32, c
         rb = {key: refb[key][b:b + 1, :, :t, :t] for key in ("retained", "legal", "margin")}
         rb.update(dq=refb["dq"][None, sl], dk=refb["dk"][None, sl], dv=refb["dv"][None, sl])
         gb = {"dq": gq[None, sl], "dk": gk[None, sl], "dv": gv[None, sl], "mask": gm[b:b + 1, :, :t, :t]}
-        parity.check_backward(gb, rb, block, fp32, causal=causal, grad_dtype=grad_dtype)
+
+        def replay(sl=sl, b=b, t=t):
+            r = orc.mala_backward_bshd(q64[None, sl], k64[None, sl], v64[None, sl], parity.to64(o_in)[None, sl],
+                                       do64[None, sl], parity.to64(lse_in)[None, :, sl], scale, tau, block, block,
+                                       causal, forced=gm[b:b + 1, :, :t, :t].astype(bool))
+            return r
+
+        parity.check_backward(gb, rb, block, fp32, causal=causal, grad_dtype=grad_dtype, replay=replay)
         legal = np.tril(np.ones((t, t), bool)) if causal else np.ones((t, t), bool)
         np.testing.assert_array_equal(bcounts[b, :, :t], (gm[b, :, :t, :t].astype(bool) & legal).sum(-2))
 
