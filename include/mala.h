@@ -160,6 +160,13 @@ size_t mala_bwd_workspace_size(int batch, int seqlen_q, int seqlen_k, int heads_
  *  retained_counts: [batch, heads_q, ceil(seqlen_k / block_k)]
  *  tile_mask:       [batch, heads_q, ceil(seqlen_q / block_q), ceil(seqlen_k / block_k)]
  *  Other arguments as for mala_fwd.
+ *
+ * Range: with bf16 inputs and head_dim 128 (the tensor-core kernel) the
+ * post-score products take fp16 operands, which hold every bf16 value of
+ * magnitude up to 65504 (exactly from 2^-17 up).  A finite q, k, v or dout
+ * element beyond 65504 sets bit 4 of the device status word
+ * (mala_device_status returns MALA_ERR_INVALID_ARG) and the gradients of that
+ * call are not valid.  fp32 inputs and the other shapes have no such limit.
  */
 mala_status mala_bwd(const void* q, const void* k, const void* v, const void* o,
                      const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -340,7 +347,9 @@ size_t mala_decode_noalloc_max_floats(void);
  * kernels set.  Bits: 1 = a bounded on-chip wait expired (the kernel gave up
  * and its outputs are not valid); 2 = mala_decode_varlen read a sequence
  * length outside [1, max_cache_len], or mala_fwd_varlen / mala_bwd_varlen
- * read sequence bounds that break their contract.  *device_code receives the raw word
+ * read sequence bounds that break their contract; 4 = a bf16 input of the
+ * tensor-core backward lies beyond fp16's range (see mala_bwd).
+ * *device_code receives the raw word
  * (0 = no event).  Returns MALA_OK (word 0), MALA_ERR_TIMEOUT (bit 1 set),
  * MALA_ERR_INVALID_ARG (any other bit), or MALA_ERR_CUDA if synchronisation
  * failed.

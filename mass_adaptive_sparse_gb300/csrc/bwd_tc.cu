@@ -566,9 +566,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   }
 }
 
+// True if one of the four bf16 values of v is finite and beyond fp16's range
+// (|x| > 65504), where the fp16 copy would become +-inf.
+__device__ __forceinline__ bool beyond_fp16(uint2 v) {
+  const float m = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))), fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+  return m > 65504.f && m <= 3.4e38f;
+}
+
 // Exact fp16 copies of q, k, v, dO (bf16 in; exact for |x| in the fp16
 // normal range), D = rowsum(O * dO), and a zeroed fp32 dQ accumulator.  One
-// warp per row; each lane converts 4 of the 128 elements.
+// warp per row; each lane converts 4 of the 128 elements.  A finite input
+// beyond fp16's range sets kStatusFp16Range (its copy would be +-inf).
 __global__ void bwd_tc_prep_kernel(const BwdArgs a, uint32_t* q16, uint32_t* k16, uint32_t* v16, uint32_t* do16) {
   const size_t lb = a.cu ? 1 : a.B;       // a packed batch is one run of Lq rows
   const size_t qrows = lb * a.Lq * a.Hq;
@@ -583,6 +591,8 @@ __global__ void bwd_tc_prep_kernel(const BwdArgs a, uint32_t* q16, uint32_t* k16
         make_uint2(pack_f16(bf16_lo(qv.x), bf16_hi(qv.x)), pack_f16(bf16_lo(qv.y), bf16_hi(qv.y)));
     reinterpret_cast<uint2*>(do16)[row * 32 + lane] =
         make_uint2(pack_f16(bf16_lo(dv.x), bf16_hi(dv.x)), pack_f16(bf16_lo(dv.y), bf16_hi(dv.y)));
+    if (__any_sync(0xffffffffu, beyond_fp16(qv) || beyond_fp16(dv)) && lane == 0)
+      atomicOr(a.status, kStatusFp16Range);
     float s = bf16_lo(ov.x) * bf16_lo(dv.x) + bf16_hi(ov.x) * bf16_hi(dv.x) +
               bf16_lo(ov.y) * bf16_lo(dv.y) + bf16_hi(ov.y) * bf16_hi(dv.y);
 #pragma unroll
@@ -603,6 +613,8 @@ __global__ void bwd_tc_prep_kernel(const BwdArgs a, uint32_t* q16, uint32_t* k16
         make_uint2(pack_f16(bf16_lo(kv.x), bf16_hi(kv.x)), pack_f16(bf16_lo(kv.y), bf16_hi(kv.y)));
     reinterpret_cast<uint2*>(v16)[row * 32 + lane] =
         make_uint2(pack_f16(bf16_lo(vv.x), bf16_hi(vv.x)), pack_f16(bf16_lo(vv.y), bf16_hi(vv.y)));
+    if (__any_sync(0xffffffffu, beyond_fp16(kv) || beyond_fp16(vv)) && lane == 0)
+      atomicOr(a.status, kStatusFp16Range);
   }
 }
 

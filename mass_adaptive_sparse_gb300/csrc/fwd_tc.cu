@@ -31,7 +31,8 @@
 //              the row max, the Eq. 3 test and the row sums need no exchange;
 //              the slot's 128 rows vote on the tile with one barrier reduction.
 // TMEM: S_0 (columns 0-127), S_1 (128-255), O_0 (256-383), O_1 (384-511).
-// P (bf16) is written over the first 64 columns of the slot's S; the next
+// P (bf16, two keys per 32-bit column) is written over the slot's consumed S:
+// keys 0-63 into its columns 0-31 and keys 64-127 into columns 64-95; the next
 // Q K^T of that slot is issued after its P V on the same tensor pipe, which
 // executes them in order.  The running max is only moved when it grows by more
 // than 2^8 (log2 units); P and l are kept relative to the max in use, which

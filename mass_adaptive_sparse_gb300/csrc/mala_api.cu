@@ -23,16 +23,27 @@ thread_local int g_last_cuda_error = 0;   // cudaError_t of this thread's last M
 
 constexpr int kMaxDevices = 64;
 
-int* status_word() {
-  static int* cache[kMaxDevices] = {};
+// Device address of a __device__ symbol on the current device, looked up once
+// per device and cached (the host-side name is only a stand-in).  Concurrent
+// first calls from several host threads store the same address; the slots
+// are atomic, so that is well defined.
+template <typename T, typename Sym>
+T* symbol_address(std::atomic<T*> (&cache)[kMaxDevices], const Sym& sym) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int*>(p);
+  T* p = cache[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, sym) != cudaSuccess) return nullptr;
+    p = static_cast<T*>(addr);
+    cache[dev].store(p, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return p;
+}
+
+int* status_word() {
+  static std::atomic<int*> cache[kMaxDevices] = {};
+  return symbol_address(cache, g_device_status);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -76,15 +87,8 @@ __device__ __align__(256) float g_decode_scratch[kNoAllocDecodeFloats];
 // Device address of g_decode_scratch on the current device, looked up once per
 // device (the host-side name is only a stand-in, not a device address).
 float* decode_scratch() {
-  static float* cache[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<float*>(p);
-  }
-  return cache[dev];
+  static std::atomic<float*> cache[kMaxDevices] = {};
+  return symbol_address(cache, g_decode_scratch);
 }
 
 // Workspace: D [B, Hq, Lq] fp32 | dQ accumulator fp32 (bf16 gradients only) |

@@ -17,7 +17,8 @@ enum Dtype : int { kBF16 = 0, kFP32 = 1 };
 // Device status word codes (bitwise OR of events).
 enum StatusCode : int {
   kStatusWaitTimeout = 1,   // an mbarrier wait ran past its time limit
-  kStatusBadLength = 2      // a variable-length sequence (decode cache length or packed prefill bounds) was invalid
+  kStatusBadLength = 2,     // a variable-length sequence (decode cache length or packed prefill bounds) was invalid
+  kStatusFp16Range = 4      // a finite bf16 input of the tensor-core backward lies beyond fp16's range (|x| > 65504)
 };
 
 // Prefill calls take either B sequences of Lq query / Lk key rows ([B, L, H, D]

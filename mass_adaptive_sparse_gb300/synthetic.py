@@ -122,6 +122,10 @@ CONFIGS = {
     "study_8k": PrefillConfig("study_8k", 1, 8, 8, 8192, 128, 128, torch.bfloat16, 3, (2.0, 4.0, 8.0), 3.0, 0.002,
                               (1.0,), 1006, target_rows=128, amp_seed=1007),
     "decode_128k": DecodeConfig("decode_128k", 8, 32, 8, 131072, 128, 128, 16, torch.bfloat16, 4, 6.0, (1.0, 0.0), 1005),
+    # the same cache (same seed) with sharper queries: amplitude 12 on the 4 planted cache rows,
+    # used to time the decode's skip path (the 128K decode workload keeps every tile)
+    "decode_128k_peaked": DecodeConfig("decode_128k_peaked", 8, 32, 8, 131072, 128, 128, 16, torch.bfloat16, 4,
+                                       12.0, (1.0, 0.0), 1005),
 }
 
 
@@ -194,3 +198,24 @@ def decode_inputs(cfg: DecodeConfig, N: int | None = None, B: int | None = None,
             q[b, h] += (cfg.amplitude * k[b, tgt, h // grp].mean(axis=0)).astype(np.float32)
     return {"q": _round(q, cfg.dtype), "k": _round(k, cfg.dtype), "v": _round(v, cfg.dtype),
             "N": N, "B": B, "seed": seed}
+
+
+def decode_query(cfg: DecodeConfig, k: torch.Tensor, seed: int | None = None) -> torch.Tensor:
+    """The query recipe of ``decode_inputs`` against a given cache k [B, N, Hkv, d]
+    (any float dtype, e.g. one already rounded to bf16): each query head
+    q = A * mean(n_targets random cache keys of its KV head) + N(0, 1), with
+    the noise and the target rows drawn from the seed exactly as
+    ``decode_inputs`` draws them.  Returns q [B, H, d] in cfg.dtype."""
+    seed = cfg.seed if seed is None else seed
+    B, N, Hkv, d = k.shape
+    H = cfg.H
+    _, _, s_noise, s_tgt = np.random.SeedSequence(seed).spawn(4)
+    q = _normal(s_noise, B * H * d).reshape(B, H, d)
+    rng_t = np.random.default_rng(s_tgt)
+    grp = H // Hkv
+    for b in range(B):
+        for h in range(H):
+            tgt = rng_t.integers(0, N, size=cfg.n_targets)
+            rows = k[b, torch.from_numpy(tgt), h // grp].to(torch.float64).numpy()
+            q[b, h] += (cfg.amplitude * rows.mean(axis=0)).astype(np.float32)
+    return _round(q, cfg.dtype)

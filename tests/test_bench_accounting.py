@@ -36,12 +36,17 @@ def test_decode_bytes_closed_form():
 
 
 def test_traffic_records_follow_their_sources():
+    """A record counts only while its kernel's source is the one it was taken
+    on: current records give their bytes, stale ones give None."""
+    import hashlib
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
     for kernel, by_workload in rec.items():
         if kernel.startswith("_"):
             continue
         for workload, r in by_workload.items():
-            assert bench._traffic(kernel, workload) == r["bytes_per_launch"]
+            src = os.path.join(bench.ROOT, "mass_adaptive_sparse_gb300", "csrc", r["source"])
+            current = hashlib.sha1(open(src, "rb").read()).hexdigest() == r["source_sha1"]
+            assert bench._traffic(kernel, workload) == (r["bytes_per_launch"] if current else None)
     assert bench._traffic("no_such_kernel", "prefill_128k") is None
 
 
