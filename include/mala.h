@@ -348,7 +348,10 @@ size_t mala_decode_noalloc_max_floats(void);
  * and its outputs are not valid); 2 = mala_decode_varlen read a sequence
  * length outside [1, max_cache_len], or mala_fwd_varlen / mala_bwd_varlen
  * read sequence bounds that break their contract; 4 = a bf16 input of the
- * tensor-core backward lies beyond fp16's range (see mala_bwd).
+ * tensor-core backward lies beyond fp16's range (see mala_bwd); 8 = only in
+ * the bounds-checked build (libmala_debug.so, compiled with -DMALA_DEBUG): a
+ * TMA box origin or global index of the tensor-core or decode kernels fell
+ * outside the extents checked on the host; the access was skipped.
  * *device_code receives the raw word
  * (0 = no event).  Returns MALA_OK (word 0), MALA_ERR_TIMEOUT (bit 1 set),
  * MALA_ERR_INVALID_ARG (any other bit), or MALA_ERR_CUDA if synchronisation

@@ -17,7 +17,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmala.so")
+# MALA_LIBRARY=debug selects the bounds-checked build (same kernels compiled
+# with -DMALA_DEBUG); anything else, or unset, the release build.
+LIB_PATH = os.path.join(_HERE, "libmala_debug.so" if os.environ.get("MALA_LIBRARY") == "debug" else "libmala.so")
 
 MALA_BF16, MALA_FP32 = 0, 1
 STATUS = {0: "MALA_OK", 1: "MALA_ERR_INVALID_ARG", 2: "MALA_ERR_UNSUPPORTED", 3: "MALA_ERR_WORKSPACE",
@@ -45,7 +47,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libmala.so not built ({LIB_PATH}); run "
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} not built ({LIB_PATH}); run "
                                "`python -m mass_adaptive_sparse_gb300.build` first")
         L = ctypes.CDLL(LIB_PATH)
         L.mala_status_string.restype = ctypes.c_char_p

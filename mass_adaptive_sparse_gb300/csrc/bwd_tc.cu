@@ -137,6 +137,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   if (kb >= Tc) return;                  // past the sequence's key blocks (packed batches)
   // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
   const int mTr = a.cu ? (a.Lmax + kBlk - 1) / kBlk : Tr, mTc = a.cu ? mTr : Tc;
+  const int lb = a.cu ? 1 : a.B;         // batch extent of the layout (a packed batch is one run of rows)
   const int ibot = a.causal ? kb : 0;
   const int ni = Tr - ibot;
   const int ntiles = G * ni;
@@ -172,10 +173,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       prefetch_tensormap(&mdo);
       const uint32_t kvf = smem_u32(&bars.kv_full);
       mbar_expect_tx(kvf, 2 * kTile);
-      tma_load_4d(sK, &mk, kvf, 0, hk, row0 + kb * kBlk, bc);
-      tma_load_4d(sK + kHalf, &mk, kvf, 64, hk, row0 + kb * kBlk, bc);
-      tma_load_4d(sV, &mv, kvf, 0, hk, row0 + kb * kBlk, bc);
-      tma_load_4d(sV + kHalf, &mv, kvf, 64, hk, row0 + kb * kBlk, bc);
+      if (dbg_box(64, hk, row0 + kb * kBlk, bc, kD, a.Hkv, row0, row0 + Lk, a.Lk, lb, a.status)) {
+        tma_load_4d(sK, &mk, kvf, 0, hk, row0 + kb * kBlk, bc);
+        tma_load_4d(sK + kHalf, &mk, kvf, 64, hk, row0 + kb * kBlk, bc);
+        tma_load_4d(sV, &mv, kvf, 0, hk, row0 + kb * kBlk, bc);
+        tma_load_4d(sV + kHalf, &mv, kvf, 64, hk, row0 + kb * kBlk, bc);
+      }
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1, n = t >> 1;
@@ -183,8 +186,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int h = hk * G + t / ni, i = ibot + t % ni;
         const uint32_t qf = smem_u32(&bars.q_full[s]);
         mbar_expect_tx(qf, kTile);
-        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row0 + i * kBlk, bc);
-        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row0 + i * kBlk, bc);
+        if (dbg_box(64, h, row0 + i * kBlk, bc, kD, a.Hq, row0, row0 + Lq, a.Lq, lb, a.status)) {
+          tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row0 + i * kBlk, bc);
+          tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row0 + i * kBlk, bc);
+        }
         ++issued;
       }
       // every issued load lands before the CTA can finish, abort or not
@@ -304,8 +309,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const int q = i * kBlk + r;
       if (q < Lq) {
         const size_t off = (static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + q;
-        n_lse = a.lse[off];
-        n_d = a.delta[off];
+        const bool in = dbg_idx(off, static_cast<size_t>(lb) * a.Hq * a.Lq, a.status);
+        n_lse = in ? a.lse[off] : 0.f;
+        n_d = in ? a.delta[off] : 0.f;
         n_thr = test ? a.log2_tau - lg2(a.causal ? static_cast<float>(q + 1) : static_cast<float>(Lk))
                      : -INFINITY;
       } else {
@@ -342,9 +348,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (release) mbar_arrive(smem_u32(&bars.dq_free));
         // two bulk groups: the first (staged in the dS buffer) is waited for alone before dS is written
         // rows past the sequence add exact zeros (their dS columns are 0)
-        if (prev_q0 < Lq) tma_reduce_add_4d(&mdq, sDS, 0, prev_h, row0 + prev_q0, bc);
+        if (prev_q0 < Lq &&
+            dbg_box(64, prev_h, row0 + prev_q0, bc, kD, a.Hq, row0, row0 + Lq, a.Lq, lb, a.status))
+          tma_reduce_add_4d(&mdq, sDS, 0, prev_h, row0 + prev_q0, bc);
         bulk_commit();
-        if (prev_q0 + 64 < Lq) tma_reduce_add_4d(&mdq, sST, 0, prev_h, row0 + prev_q0 + 64, bc);
+        if (prev_q0 + 64 < Lq &&
+            dbg_box(64, prev_h, row0 + prev_q0 + 64, bc, kD, a.Hq, row0, row0 + Lq, a.Lq, lb, a.status))
+          tma_reduce_add_4d(&mdq, sST, 0, prev_h, row0 + prev_q0 + 64, bc);
         bulk_commit();
       }
       return true;
@@ -405,11 +415,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       // an abort is caught at the vote after P^T is stored, or (skipped tiles)
       // by the next tile's waits, which return at once once the flag is up
       const int keep = named_vote_or(1, kMath, keep_row && ok);
-      uint8_t* mrow = a.mask ? a.mask + ((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb : nullptr;
+      const size_t mrow_i = ((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb;
+      uint8_t* mrow = a.mask && dbg_idx(mrow_i, static_cast<size_t>(a.B) * a.Hq * mTr * mTc, a.status)
+                          ? a.mask + mrow_i : nullptr;
       if (tid == 0) {
         head_kept += keep;
         if (i == Tr - 1) {                        // last query block of this head
-          if (a.counts != nullptr) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTc + kb] = head_kept;
+          if (a.counts != nullptr &&
+              dbg_idx((static_cast<size_t>(b) * a.Hq + h) * mTc + kb, static_cast<size_t>(a.B) * a.Hq * mTc, a.status))
+            a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTc + kb] = head_kept;
           head_kept = 0;
         }
       }
@@ -437,8 +451,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (ok) {
           const uint32_t df = smem_u32(&bars.do_full);
           mbar_expect_tx(df, kTile);
-          tma_load_4d(sDO, &mdo, df, 0, h, row0 + q0, bc);
-          tma_load_4d(sDO + kHalf, &mdo, df, 64, h, row0 + q0, bc);
+          if (dbg_box(64, h, row0 + q0, bc, kD, a.Hq, row0, row0 + Lq, a.Lq, lb, a.status)) {
+            tma_load_4d(sDO, &mdo, df, 0, h, row0 + q0, bc);
+            tma_load_4d(sDO + kHalf, &mdo, df, 64, h, row0 + q0, bc);
+          }
           ++do_issued;
         }
       }
@@ -539,6 +555,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       const size_t off = ((static_cast<size_t>(bc) * a.Lk + row0 + (key_ok ? key : 0)) * a.Hkv + hk) * kD + 64 * cg;
       Tg* dvp = static_cast<Tg*>(a.dv) + off;
       Tg* dkp = static_cast<Tg*>(a.dk) + off;
+      const bool store = key_ok && dbg_idx(off + 63, static_cast<size_t>(lb) * a.Lk * a.Hkv * kD, a.status);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
@@ -548,9 +565,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
-        if (key_ok) store_grad_row<Tg>(dvp + c * 32, v, 1.f);
+        if (store) store_grad_row<Tg>(dvp + c * 32, v, 1.f);
         if (nret > 0) tmem_ld32_sync(lane_addr + kColDK + 64 * cg + c * 32, v);
-        if (key_ok) store_grad_row<Tg>(dkp + c * 32, v, 1.f);
+        if (store) store_grad_row<Tg>(dkp + c * 32, v, 1.f);
       }
     }
     // a dO load issued for an abandoned tile must land before the CTA exits

@@ -127,8 +127,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
         const int row = (t1 - 1 - t) * kBK;                 // newest tile first
         const uint32_t kf = smem_u32(&bars.k_full[s]);
         mbar_expect_tx(kf, kTile);
-        tma_load_4d(sK + s * kTile, &mk, kf, 0, hk, row, b);
-        tma_load_4d(sK + s * kTile + kHalf, &mk, kf, 64, hk, row, b);
+        if (dbg_box(64, hk, row, b, kD, a.Hkv, 0, n_b, a.N, a.B, a.status)) {
+          tma_load_4d(sK + s * kTile, &mk, kf, 0, hk, row, b);
+          tma_load_4d(sK + s * kTile + kHalf, &mk, kf, 64, hk, row, b);
+        }
         ++issued;
       }
       int never = 0;      // in-flight K loads must land before exit, abort or not
@@ -190,7 +192,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
           const int d = 32 * pw + 16 * mt + gq + 8 * hrow;
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            if (2 * cq + e < G) split_record(a, sp, b, hk * G + 2 * cq + e)[4 + d] = o[mt][2 * hrow + e];
+            if (2 * cq + e < G &&
+                dbg_idx(((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + 2 * cq + e) * (kD + 4) + 4 + d,
+                        static_cast<size_t>(a.splits) * a.B * a.Hq * (kD + 4), a.status))
+              split_record(a, sp, b, hk * G + 2 * cq + e)[4 + d] = o[mt][2 * hrow + e];
         }
     }
     named_sync(2, 256);
@@ -278,8 +283,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     // head g's own decision: in the group variant every head follows the group
     const bool own_g = a.per_head ? (!test || keep_g) : keep;
     if (a.mask != nullptr) {
-      if (!a.per_head && tid == 0) a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
-      if (a.per_head && tid < G) a.mask[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * Tmax + j] = own_g ? 1 : 0;
+      if (!a.per_head && tid == 0 &&
+          dbg_idx((static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j, static_cast<size_t>(a.B) * a.Hkv * Tmax, a.status))
+        a.mask[(static_cast<size_t>(b) * a.Hkv + hk) * Tmax + j] = keep ? 1 : 0;
+      if (a.per_head && tid < G &&
+          dbg_idx((static_cast<size_t>(b) * a.Hq + hk * G + tid) * Tmax + j, static_cast<size_t>(a.B) * a.Hq * Tmax,
+                  a.status))
+        a.mask[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * Tmax + j] = own_g ? 1 : 0;
     }
     if (!keep) continue;
     ++kept;
@@ -291,8 +301,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     if (tid == 96) {
       const uint32_t vf = smem_u32(&bars.v_full[vs]);
       mbar_expect_tx(vf, kTile);
-      tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBK, b);
-      tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBK, b);
+      if (dbg_box(64, hk, j * kBK, b, kD, a.Hkv, 0, n_b, a.N, a.B, a.status)) {
+        tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, j * kBK, b);
+        tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, j * kBK, b);
+      }
     }
     // lazily moved reference max (lane g), broadcast for this thread's heads 2cq, 2cq+1
     float alpha_g = 1.f;
@@ -350,7 +362,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     xlr[warp][2 * cq] = lr0; xlr[warp][2 * cq + 1] = lr1;
   }
   named_sync(1, 128);
-  if (warp == 0 && lane < G && !*abortp) {
+  if (warp == 0 && lane < G && !*abortp &&
+      dbg_idx(((static_cast<size_t>(sp) * a.B + b) * a.Hq + hk * G + lane) * (kD + 4) + 3,
+              static_cast<size_t>(a.splits) * a.B * a.Hq * (kD + 4), a.status)) {
     float* rec = split_record(a, sp, b, hk * G + lane);
     rec[0] = m_g;
     rec[1] = (xl[2][0][lane] + xl[2][1][lane]) + (xl[2][2][lane] + xl[2][3][lane]);
@@ -358,8 +372,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     rec[3] = 0.f;
   }
   if (a.counts != nullptr && !*abortp) {
-    if (!a.per_head && tid == 0) a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
-    if (a.per_head && tid < G) a.counts[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * a.splits + sp] = kept_g;
+    if (!a.per_head && tid == 0 &&
+        dbg_idx((static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp, static_cast<size_t>(a.B) * a.Hkv * a.splits,
+                a.status))
+      a.counts[(static_cast<size_t>(b) * a.Hkv + hk) * a.splits + sp] = kept;
+    if (a.per_head && tid < G &&
+        dbg_idx((static_cast<size_t>(b) * a.Hq + hk * G + tid) * a.splits + sp, static_cast<size_t>(a.B) * a.Hq * a.splits,
+                a.status))
+      a.counts[(static_cast<size_t>(b) * a.Hq + hk * G + tid) * a.splits + sp] = kept_g;
   }
   named_sync(2, 256);
   // V loads issued but never consumed (abort path) must land before exit; these

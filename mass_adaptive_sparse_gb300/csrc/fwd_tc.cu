@@ -144,6 +144,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
   const int Tr = (Lq + kBlk - 1) / kBlk, Tc = (Lk + kBlk - 1) / kBlk;
   // tile rows / columns of mask and counts (a packed batch pads each sequence to Lmax)
   const int mTr = a.cu ? (a.Lmax + kBlk - 1) / kBlk : Tr, mTc = a.cu ? mTr : Tc;
+  const int lb = a.cu ? 1 : a.B;         // batch extent of the layout (a packed batch is one run of rows)
   const int pair = (Tr + 1) / 2 - 1 - static_cast<int>(blockIdx.y);   // heaviest pairs first
   if (pair < 0) return;                  // past the sequence's query blocks (packed batches)
   const int nslots = (2 * pair + 1 < Tr) ? 2 : 1;
@@ -200,8 +201,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       mbar_expect_tx(qf, kTile * nslots);
       for (int s = 0; s < nslots; ++s) {
         const int row = row0 + (2 * pair + s) * kBlk;
-        tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, bc);
-        tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, bc);
+        if (dbg_box(64, h, row, bc, kD, a.Hq, row0, row0 + Lq, a.Lq, lb, a.status)) {
+          tma_load_4d(sQ + s * kTile, &mq, qf, 0, h, row, bc);
+          tma_load_4d(sQ + s * kTile + kHalf, &mq, qf, 64, h, row, bc);
+        }
       }
       // test hook (failure detection): CTA (0, 0) leaves its first K tile
       // unloaded, so the waits for it expire and the CTA gives up
@@ -214,8 +217,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           const uint32_t kf = smem_u32(&bars.k_full[st]);
           const int row = row0 + (jtop - t) * kBlk;
           mbar_expect_tx(kf, kTile);
-          tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, bc);
-          tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, bc);
+          if (dbg_box(64, hk, row, bc, kD, a.Hkv, row0, row0 + Lk, a.Lk, lb, a.status)) {
+            tma_load_4d(sK + st * kTile, &mk, kf, 0, hk, row, bc);
+            tma_load_4d(sK + st * kTile + kHalf, &mk, kf, 64, hk, row, bc);
+          }
         }
         ++issued;
       }
@@ -244,8 +249,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             if (ok) {
               const uint32_t vf = smem_u32(&bars.v_full[vs]);
               mbar_expect_tx(vf, kTile);
-              tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, row0 + (jtop - t) * kBlk, bc);
-              tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, row0 + (jtop - t) * kBlk, bc);
+              const int row = row0 + (jtop - t) * kBlk;
+              if (dbg_box(64, hk, row, bc, kD, a.Hkv, row0, row0 + Lk, a.Lk, lb, a.status)) {
+                tma_load_4d(sV + vs * kTile, &mv, vf, 0, hk, row, bc);
+                tma_load_4d(sV + vs * kTile + kHalf, &mv, vf, 64, hk, row, bc);
+              }
               load = true;
               armed = t;
             }
@@ -414,7 +422,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int u = it - 1;                   // local step of this slot
         if (r == 0) {
           keep_flag[s][u & 1] = keep;
-          if (mask_row) mask_row[j] = static_cast<uint8_t>(keep);
+          if (mask_row && dbg_idx(((static_cast<size_t>(b) * a.Hq + h) * mTr + qb) * mTc + j,
+                                  static_cast<size_t>(a.B) * a.Hq * mTr * mTc, a.status))
+            mask_row[j] = static_cast<uint8_t>(keep);
           mbar_arrive(smem_u32(&bars.dec[s][u & 1]));
         }
         if (!keep) continue;
@@ -468,17 +478,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.o_done[s]), 0, abortp, a.status) && ok;
       fence_after_sync();
       if (__all_sync(0xffffffffu, ok && !*abortp)) {
-        Tout* orow = static_cast<Tout*>(a.o) +
-                     ((static_cast<size_t>(bc) * a.Lq + row0 + (valid ? qrow : 0)) * a.Hq + h) * kD;
+        const size_t orow_i = ((static_cast<size_t>(bc) * a.Lq + row0 + (valid ? qrow : 0)) * a.Hq + h) * kD;
+        Tout* orow = static_cast<Tout*>(a.o) + orow_i;
+        const bool store = valid && dbg_idx(orow_i + kD - 1, static_cast<size_t>(lb) * a.Lq * a.Hq * kD, a.status) &&
+                           dbg_idx((static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow,
+                                   static_cast<size_t>(lb) * a.Hq * a.Lq, a.status);
         const float inv = 1.f / lr;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
           tmem_ld32_sync(lane_addr + colO + c * 32, reinterpret_cast<uint32_t*>(o));
-          if (valid) store_row<Tout>(orow + c * 32, o, inv);
+          if (store) store_row<Tout>(orow + c * 32, o, inv);
         }
-        if (valid) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m_used + log2f(l)) * kLn2;
-        if (a.counts != nullptr && r == 0) a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTr + qb] = nret;
+        if (store) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m_used + log2f(l)) * kLn2;
+        if (a.counts != nullptr && r == 0 &&
+            dbg_idx((static_cast<size_t>(b) * a.Hq + h) * mTr + qb, static_cast<size_t>(a.B) * a.Hq * mTr, a.status))
+          a.counts[(static_cast<size_t>(b) * a.Hq + h) * mTr + qb] = nret;
       }
       fence_before_sync();
     }

@@ -18,8 +18,35 @@ enum Dtype : int { kBF16 = 0, kFP32 = 1 };
 enum StatusCode : int {
   kStatusWaitTimeout = 1,   // an mbarrier wait ran past its time limit
   kStatusBadLength = 2,     // a variable-length sequence (decode cache length or packed prefill bounds) was invalid
-  kStatusFp16Range = 4      // a finite bf16 input of the tensor-core backward lies beyond fp16's range (|x| > 65504)
+  kStatusFp16Range = 4,     // a finite bf16 input of the tensor-core backward lies beyond fp16's range (|x| > 65504)
+  kStatusDebugBounds = 8    // bounds-checked build only: a TMA coordinate or global index out of range (skipped)
 };
+
+// Bounds checks of the bounds-checked build (-DMALA_DEBUG): every TMA box
+// origin and global index is checked against the extents the host validated;
+// a violation sets kStatusDebugBounds and the caller skips the access (a
+// skipped load ends in an expired, bounded wait, never a fault).  In the
+// release build the checks are constant true and compile away.
+#ifdef __CUDACC__
+#ifdef MALA_DEBUG
+__device__ __forceinline__ bool dbg_ok(bool ok, int* status) {
+  if (!ok) atomicOr(status, kStatusDebugBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool dbg_ok(bool, int*) { return true; }
+#endif
+// index < n (a flat global index against its buffer's element count)
+__device__ __forceinline__ bool dbg_idx(size_t index, size_t n, int* status) { return dbg_ok(index < n, status); }
+// Origin (x, h, row, b) of a TMA box over a [B, rows, H, D] tensor whose
+// current sequence spans rows [lo, hi): x a multiple of 8 elements (16 bytes
+// of 16-bit data) inside D, h and b in range, row inside [lo, hi) and hi <= rows.
+__device__ __forceinline__ bool dbg_box(int x, int h, int row, int b, int D, int H, int lo, int hi, int rows, int B,
+                                        int* status) {
+  return dbg_ok(x >= 0 && x % 8 == 0 && x < D && h >= 0 && h < H && b >= 0 && b < B && row >= lo && row < hi &&
+                hi <= rows, status);
+}
+#endif
 
 // Prefill calls take either B sequences of Lq query / Lk key rows ([B, L, H, D]
 // tensors, cu == null), or B sequences of different lengths packed along one

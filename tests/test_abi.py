@@ -35,6 +35,16 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(api.EXPORTS)
 
 
+def test_bounds_checked_build_exports_the_same_symbols():
+    """libmala_debug.so (the -DMALA_DEBUG build) is a drop-in for libmala.so."""
+    from mass_adaptive_sparse_gb300 import build
+    if not os.path.exists(build.LIB_DEBUG):
+        build.build(variants=("debug",))
+    dbg = ctypes.CDLL(build.LIB_DEBUG)
+    for n in declared_entry_points():
+        assert hasattr(dbg, n), f"{n} not exported by libmala_debug.so"
+
+
 def test_status_strings(lib):
     for code, name in api.STATUS.items():
         assert lib.mala_status_string(code).decode() == name
