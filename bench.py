@@ -444,13 +444,13 @@ def main():
 
         s_in, s_cmp, s_dec, s_out = (torch.cuda.Stream(dev) for _ in range(4))
 
-        def ev(st_):
-            e_ = torch.cuda.Event()
+        def ev(st_, timing=False):
+            e_ = torch.cuda.Event(enable_timing=timing)
             e_.record(st_)
             return e_
 
-        def e2e_step():
-            start = ev(stream)
+        def e2e_step(stamps=None):
+            start = ev(stream, stamps is not None)
             for st_ in (s_in, s_cmp, s_dec, s_out):
                 st_.wait_event(start)
             with torch.cuda.stream(s_in):
@@ -491,23 +491,48 @@ def main():
                 s_out.wait_event(done_d)
                 for n in ("od", "lsed"):
                     dec_out[n].copy_(d[n], non_blocking=True)
-            for st_ in (s_in, s_cmp, s_dec, s_out):
-                stream.wait_event(ev(st_))
+            ends = [ev(st_, stamps is not None) for st_ in (s_in, s_cmp, s_dec, s_out)]
+            for e_ in ends:
+                stream.wait_event(e_)
+            if stamps is not None:
+                stamps.extend([start] + ends)
 
         e2e_step()
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e2e = max(1, min(args.steps, 5))
-        e0.record(stream)
-        for _ in range(n_e2e):
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+        es[0].record(stream)
+        for i in range(n_e2e):
             e2e_step()
-        e1.record(stream)
+            es[i + 1].record(stream)
         barrier()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
+        per_step = [es[i].elapsed_time(es[i + 1]) for i in range(n_e2e)]
+        e2e_ms = max_over_ranks(statistics.mean(per_step))
+        # diagnostics, outside the timed region: when each stream finished its
+        # part of one more step, and the plain pinned-copy bandwidth of this machine
+        stamps = []
+        e2e_step(stamps)
+        torch.cuda.synchronize()
+        stream_ms = {n: stamps[0].elapsed_time(e_) for n, e_ in zip(("copies_in", "compute", "decode", "copies_out"),
+                                                                     stamps[1:])}
+        probe = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+        probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        bw = {}
+        for name, dst, src in (("h2d_gbs", probe_d, probe), ("d2h_gbs", probe, probe_d)):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            dst.copy_(src, non_blocking=True)
+            c0.record(stream)
+            for _ in range(3):
+                dst.copy_(src, non_blocking=True)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            bw[name] = 3 * (1 << 30) / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        del probe, probe_d
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e,
+               "steps": n_e2e, "step_ms": per_step,
                "pipeline": f"prefill in {nchunk} head chunks; copies in, compute, decode and copies out on "
-                           "four streams"}
+                           "four streams",
+               "stream_end_ms": stream_ms, "pinned_copy": bw}
         del chunks
 
     if not ranks.reports:

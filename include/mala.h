@@ -58,7 +58,8 @@ extern "C" {
 typedef enum {
   MALA_OK = 0,
   MALA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, tau < 0 or NaN */
-  MALA_ERR_UNSUPPORTED = 2,  /* well-formed but not built: head_dim, tile size, dtype */
+  MALA_ERR_UNSUPPORTED = 2,  /* well-formed but not built: head_dim, tile size, dtype, or more than
+                                2^31 - 1 CTAs (batch x heads_q x tiles along the longer sequence) */
   MALA_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the *_workspace_size() */
   MALA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
   MALA_ERR_TIMEOUT = 5       /* a bounded device-side wait expired (device status) */

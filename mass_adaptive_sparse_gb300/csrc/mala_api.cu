@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -71,6 +72,9 @@ mala_status check_prefill(int batch, int seqlen_q, int seqlen_k, int heads_q, in
   if (head_dim < 1) return MALA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return MALA_ERR_UNSUPPORTED;
   if (block_q != block_k || (block_q != 64 && block_q != 128)) return MALA_ERR_UNSUPPORTED;
+  // the kernels number their CTAs (batch x heads x tile rows or columns) with 32-bit ints
+  const int64_t tiles = (static_cast<int64_t>(seqlen_q > seqlen_k ? seqlen_q : seqlen_k) + block_q - 1) / block_q;
+  if (static_cast<int64_t>(batch) * heads_q * tiles > INT32_MAX) return MALA_ERR_UNSUPPORTED;
   return MALA_OK;
 }
 

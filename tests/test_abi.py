@@ -77,6 +77,8 @@ def _fwd(lib, q=FAKE, B=1, L=256, Hq=2, Hkv=2, D=64, dt=1, causal=1, bq=64, bk=6
     (dict(dt=7), 1), (dict(causal=2), 1), (dict(Lk=300), 1), (dict(tau=-1.0), 1),
     (dict(tau=float("nan")), 1), (dict(tau=float("inf")), 1), (dict(scale=0.0), 1),
     (dict(D=96), 2), (dict(bq=64, bk=128), 2), (dict(bq=32, bk=32), 2),
+    # more CTAs (batch x heads x tiles) than 32-bit CTA numbering holds
+    (dict(B=65535, Hq=65535, Hkv=65535, L=128, bq=64, bk=64), 2),
 ])
 def test_fwd_rejects_bad_arguments(lib, kw, code):
     assert _fwd(lib, **kw) == code
