@@ -71,29 +71,18 @@ struct Bars {
   uint64_t fin[2];        // every MMA of a sequencer complete (its own wait before exit)
 };
 
+// Four consecutive output values to global memory (8 bytes of bf16, 16 of fp32).
 template <typename Tout>
-__device__ __forceinline__ void store_row(Tout* dst, const float* v, float scale);
+__device__ __forceinline__ void store_out4(Tout* dst, float4 x);
 
 template <>
-__device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, const float* v, float scale) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 w;
-    w.x = pack_bf16(v[8 * i + 0] * scale, v[8 * i + 1] * scale);
-    w.y = pack_bf16(v[8 * i + 2] * scale, v[8 * i + 3] * scale);
-    w.z = pack_bf16(v[8 * i + 4] * scale, v[8 * i + 5] * scale);
-    w.w = pack_bf16(v[8 * i + 6] * scale, v[8 * i + 7] * scale);
-    d4[i] = w;
-  }
+__device__ __forceinline__ void store_out4<__nv_bfloat16>(__nv_bfloat16* dst, float4 x) {
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
 }
 
 template <>
-__device__ __forceinline__ void store_row<float>(float* dst, const float* v, float scale) {
-  float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    d4[i] = make_float4(v[4 * i] * scale, v[4 * i + 1] * scale, v[4 * i + 2] * scale, v[4 * i + 3] * scale);
+__device__ __forceinline__ void store_out4<float>(float* dst, float4 x) {
+  *reinterpret_cast<float4*>(dst) = x;
 }
 
 // Scores of the columns past `last` (the last legal one) become -inf.
@@ -117,6 +106,44 @@ __device__ __forceinline__ void exp_pack(uint32_t* sr, uint64_t nsc2, uint64_t n
     acc = add2(acc, f2(p0, p1));
     add_bf16x2(r0, r1, w);
     sr[c] = w;
+  }
+}
+
+// Epilogue of a softmax warp: its 32 query rows of O / l (128 columns) leave
+// TMEM 32 columns at a time through a padded shared-memory tile (rows 36 floats
+// apart: the row-wise float4 writes and the four-rows-at-a-time float4 reads
+// both take the minimum four wavefronts), so that each global store
+// instruction writes four whole row segments rather than 32 scattered pieces.
+// `stage` is the slot's Q buffer, free once the slot's products are done.  Not
+// inlined: that keeps the main loop's code as it was (0.4 ms faster at 128K
+// than the inlined form).  o_out: [lb, seqlen_q, heads_q, 128] of Tout; rows at
+// or past Lq are not written.
+template <typename Tout>
+__device__ __noinline__ void write_o(uint8_t* smem_raw, uint32_t stage, int warp, int lane, int qb, int Lq, int row0,
+                                     int bc, int h, int lb, int seqlen_q, int heads_q, void* o_out, uint32_t o_taddr,
+                                     float inv, int* status) {
+  fence_proxy_async_smem();
+  float* tp = reinterpret_cast<float*>(smem_raw + (stage - smem_u32(smem_raw))) + (warp & 3) * (32 * 36);
+  const int rr0 = lane >> 3, cc = 4 * (lane & 7);
+  const size_t o_elems = static_cast<size_t>(lb) * seqlen_q * heads_q * kD;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float o[32];
+    tmem_ld32_sync(o_taddr + c * 32, reinterpret_cast<uint32_t*>(o));
+    float4* w4 = reinterpret_cast<float4*>(tp + lane * 36);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      w4[u] = make_float4(o[4 * u] * inv, o[4 * u + 1] * inv, o[4 * u + 2] * inv, o[4 * u + 3] * inv);
+    __syncwarp();
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const int rr = 4 * k4 + rr0;
+      const int qr = qb * kBlk + 32 * (warp & 3) + rr;
+      const float4 x = *reinterpret_cast<const float4*>(tp + rr * 36 + cc);
+      const size_t off = ((static_cast<size_t>(bc) * seqlen_q + row0 + qr) * heads_q + h) * kD + 32 * c + cc;
+      if (qr < Lq && dbg_idx(off + 3, o_elems, status)) store_out4<Tout>(static_cast<Tout*>(o_out) + off, x);
+    }
+    __syncwarp();
   }
 }
 
@@ -486,18 +513,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       ok = mbar_wait(smem_u32(&bars.o_done[s]), 0, abortp, a.status) && ok;
       fence_after_sync();
       if (__all_sync(0xffffffffu, ok && !*abortp)) {
-        const size_t orow_i = ((static_cast<size_t>(bc) * a.Lq + row0 + (valid ? qrow : 0)) * a.Hq + h) * kD;
-        Tout* orow = static_cast<Tout*>(a.o) + orow_i;
-        const bool store = valid && dbg_idx(orow_i + kD - 1, static_cast<size_t>(lb) * a.Lq * a.Hq * kD, a.status) &&
-                           dbg_idx((static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow,
-                                   static_cast<size_t>(lb) * a.Hq * a.Lq, a.status);
+        const bool store = valid && dbg_idx((static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow,
+                                            static_cast<size_t>(lb) * a.Hq * a.Lq, a.status);
         const float inv = 1.f / lr;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          tmem_ld32_sync(lane_addr + colO + c * 32, reinterpret_cast<uint32_t*>(o));
-          if (store) store_row<Tout>(orow + c * 32, o, inv);
-        }
+        write_o<Tout>(smem_raw, sQ + s * kTile, warp, lane, qb, Lq, row0, bc, h, lb, a.Lq, a.Hq, a.o, lane_addr + colO, inv,
+                      a.status);
         if (store) a.lse[(static_cast<size_t>(bc) * a.Hq + h) * a.Lq + row0 + qrow] = (m_used + log2f(l)) * kLn2;
         if (a.counts != nullptr && r == 0 &&
             dbg_idx((static_cast<size_t>(b) * a.Hq + h) * mTr + qb, static_cast<size_t>(a.B) * a.Hq * mTr, a.status))

@@ -36,6 +36,12 @@ LSE_ABS = 1e-3
 ZERO_REF_MEAN = 1e-6      # below this mean |ref| the mean relative error is undefined
 MAX_FLIPPED_FRACTION = 0.01
 
+# How often the checks met a borderline disagreement and replayed (reported at
+# the end of the run by tests/conftest.py): units compared, units replayed,
+# borderline tiles the replay took the other way from the oracle's own test.
+REPLAY_STATS = {"fwd_blocks": 0, "fwd_replayed": 0, "decode_rows": 0, "decode_replayed": 0,
+                "bwd_tiles": 0, "bwd_replayed_tiles": 0, "overridden_tiles": 0}
+
 
 def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
@@ -143,6 +149,9 @@ def check_forward(gpu_o, gpu_lse, gpu_mask, ref, q, k, v, scale, tau, block, out
             for i in blocks:
                 rows_ok[b, h, i * block:min(L, (i + 1) * block)] = True
     n_blocks = B * len(heads) * len(blocks)
+    REPLAY_STATS["fwd_blocks"] += n_blocks
+    REPLAY_STATS["fwd_replayed"] += replayed
+    REPLAY_STATS["overridden_tiles"] += overridden
     assert replayed <= max(1, MAX_FLIPPED_FRACTION * n_blocks), f"{replayed} of {n_blocks} blocks replayed"
     sel = np.transpose(rows_ok, (0, 2, 1))               # [B, L, H]
     metrics = check_close("o", gpu_o[sel], exp_o[sel], out_dtype, fp32=fp32)
@@ -163,12 +172,15 @@ def decode_expected(gpu_mask, ref_o, ref_lse, ref_retained, q, k, v, scale, tau,
     decision must equal the replay's; the replay's O and lse are then the
     expected values.  Returns (o, lse, replayed)."""
     g = np.asarray(gpu_mask, bool)
+    REPLAY_STATS["decode_rows"] += 1
     if not (g != np.asarray(ref_retained, bool)).any():
         return ref_o, ref_lse, False
+    REPLAY_STATS["decode_replayed"] += 1
     rep = orc.mala_decode(q, k, v, scale, tau, block, splits, forced=g)
     bad = g != rep.retained
     assert not bad.any(), (f"decode tiles {np.flatnonzero(bad).tolist()} decided differently from the oracle's "
                            f"replay of the GPU's borderline decisions; margins {rep.margin[bad]}")
+    REPLAY_STATS["overridden_tiles"] += int(rep.overridden.sum())
     return rep.o, rep.lse, True
 
 
@@ -197,6 +209,8 @@ def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=Tru
     gmask = gpu["mask"].astype(bool)
     diff = (gmask != ref["retained"]) & ref["legal"]
     metrics = {"replayed_tiles": int(diff.sum())}
+    REPLAY_STATS["bwd_tiles"] += int(ref["legal"].sum())
+    REPLAY_STATS["bwd_replayed_tiles"] += int(diff.sum())
     if diff.any():
         assert replay is not None, "the GPU decided backward tiles differently and no replay was given"
         assert diff.sum() <= max(1, MAX_FLIPPED_FRACTION * ref["legal"].sum())
@@ -207,6 +221,7 @@ def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=Tru
             raise AssertionError(f"{int(bad.sum())} bwd tiles decided differently from the oracle's replay, e.g. "
                                  f"(b={b}, h={h}, i={i}, j={j}) with margin {ref['margin'][b, h, i, j]:.4g}")
         metrics["overridden_tiles"] = int(ref["overridden"].sum())
+        REPLAY_STATS["overridden_tiles"] += metrics["overridden_tiles"]
     for name, ok in (("dq", okq), ("dk", okk), ("dv", okk)):
         if grad_dtype == torch.bfloat16:
             metrics[name] = check_close_bf16_rounded(name, gpu[name][ok], ref[name][ok])
