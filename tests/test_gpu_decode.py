@@ -101,10 +101,10 @@ def test_decode_tau0_is_dense_for_any_split():
 
 def test_decode_128k_full_size_sampled():
     """Batch 8, 32 query heads over 8 KV heads, 131072-token cache, 16 splits;
-    sequences 0 and 5 are compared with the oracle."""
+    sequences 0 and 5 (tau = 1) and 3 and 7 (tau = 0) are compared with the oracle."""
     cfg = synthetic.CONFIGS["decode_128k"]
-    for tau in (1.0, 0.0):
-        _check(cfg, cfg.N, cfg.B, tau, cfg.num_splits, cfg.block, cfg.seed, batches=[0, 5])
+    for tau, seqs in ((1.0, [0, 5]), (0.0, [3, 7])):
+        _check(cfg, cfg.N, cfg.B, tau, cfg.num_splits, cfg.block, cfg.seed, batches=seqs)
 
 
 @pytest.mark.parametrize("tau", [1.0, 0.0])
