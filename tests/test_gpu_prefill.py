@@ -168,6 +168,14 @@ def test_bf16_batch2_gqa():
     _run_case(cfg, 700, 1.0, 43, block=128)
 
 
+def test_bf16_gqa_group_of_8():
+    """16 query heads over 2 KV heads (group 8, the paper's model shares each KV
+    head among 8 query heads), ragged length, tau = 1 and 4."""
+    cfg = synthetic.PrefillConfig("gqa8", 1, 16, 2, 900, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.01)
+    for tau in (1.0, 4.0):
+        _run_case(cfg, 900, tau, 53, block=128)
+
+
 @pytest.mark.parametrize("L,lk", [(300, 700), (640, 256)])
 @pytest.mark.parametrize("tau", [1.0, 64.0])
 def test_bf16_noncausal(L, lk, tau):
