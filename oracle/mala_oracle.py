@@ -707,7 +707,7 @@ def matched_work_allocation(counts, scope):
     indices: every copy of the cell gets floor(average), and the e copies
     x with (x - cell) mod n < e get one more, where n is the number of copies
     and e the cell's remaining units.  So every cell, and the whole, executes
-    exactly MALA's total (the paper's "data-independent integer rounding").
+    exactly MALA's total (App. C.2 rounds to integers without looking at the data).
     Copies are numbered input-major: x = i for head_position, i * H + h for
     position; cells are numbered h * Tr + query block, or the query block.
     """
