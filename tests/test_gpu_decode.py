@@ -13,13 +13,17 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None, lens=None, per_head=False):
+def _check(cfg, N, B, tau, splits, block, seed, batches=None, dtype=None, d=None, lens=None, per_head=False,
+           query_cfg=None):
     """Decode on the GPU and compare with the oracle; `lens` (one cache length
     per sequence, each in [1, N]) selects the variable-length entry point over
     caches padded to N, `per_head` the entry point whose query heads decide
-    alone (masks and counts per query head)."""
+    alone (masks and counts per query head), `query_cfg` another workload's
+    query recipe over this workload's cache."""
     x = synthetic.decode_inputs(cfg, N=N, B=B, seed=seed)
     q, k, v = x["q"], x["k"], x["v"]
+    if query_cfg is not None:
+        q = synthetic.decode_query(query_cfg, k)
     if d is not None:
         q, k, v = q[..., :d].contiguous(), k[..., :d].contiguous(), v[..., :d].contiguous()
     if dtype is not None:
@@ -105,6 +109,19 @@ def test_decode_128k_full_size_sampled():
     cfg = synthetic.CONFIGS["decode_128k"]
     for tau, seqs in ((1.0, [0, 5]), (0.0, [3, 7])):
         _check(cfg, cfg.N, cfg.B, tau, cfg.num_splits, cfg.block, cfg.seed, batches=seqs)
+
+
+@pytest.mark.parametrize("splits", [2, 16])
+def test_decode_128k_peaked_sampled(splits):
+    """The sharper queries (amplitude 12 on the same planted rows) over the 128K
+    decode cache, where a split that has met its targets skips older V tiles:
+    sequences 1 and 6 at tau = 1 compared with the oracle; with 2 splits some
+    tiles are skipped."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    _, mask = _check(cfg, cfg.N, cfg.B, 1.0, splits, cfg.block, cfg.seed, batches=[1, 6],
+                     query_cfg=synthetic.CONFIGS["decode_128k_peaked"])
+    if splits == 2:
+        assert not mask[[1, 6]].all()
 
 
 @pytest.mark.parametrize("tau", [1.0, 0.0])
