@@ -453,6 +453,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       // an abort is caught at the vote after P^T is stored, or (skipped tiles)
       // by the next tile's waits, which return at once once the flag is up
       const int keep = named_vote_or(1, kMath, keep_row && ok);
+      // the decision goes to the MMA warp first: a skipped tile's successor waits on it
+      if (tid == 0) {
+        flag = keep;
+        mbar_arrive(smem_u32(&bars.dec));
+      }
       const size_t mrow_i = ((static_cast<size_t>(b) * a.Hq + h) * mTr + i) * mTc + kb;
       uint8_t* mrow = a.mask && dbg_idx(mrow_i, static_cast<size_t>(a.B) * a.Hq * mTr * mTc, a.status)
                           ? a.mask + mrow_i : nullptr;
@@ -466,11 +471,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
       }
       if (!keep) {
-        if (tid == 0) {
-          if (mrow) *mrow = 0;
-          flag = 0;
-          mbar_arrive(smem_u32(&bars.dec));
-        }
+        if (tid == 0 && mrow) *mrow = 0;
         // the previous retained tile's dQ is read out here too: the MMA warp
         // waits for it before the scores of tile t + 1 go into its region
         if (nret > flushed) {
@@ -481,8 +482,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       }
       if (tid == 0) {
         if (mrow) *mrow = 1;
-        flag = 1;
-        mbar_arrive(smem_u32(&bars.dec));
         // dO of this tile, loaded only now that the tile is retained.  The
         // buffer is free: the previous kept tile's dV and dP^T read it, and
         // every math thread has already seen that dP^T complete (dV runs first).
