@@ -265,6 +265,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int ret = flag;
         const uint32_t qb = sQ + (t & 1) * kTile;
         const uint32_t rg = tmem + region(t);
+        // a skipped tile's Q slot is free at once: its scores are complete (the
+        // vote came after them), and the producer can start the next load now
+        if (!ret) mbar_arrive(smem_u32(&bars.q_empty[t & 1]));
         if (ret) {
           if (!mbar_wait(smem_u32(&bars.do_full), nret & 1, abortp, a.status) ||
               !mbar_wait(smem_u32(&bars.p_ready), nret & 1, abortp, a.status))
@@ -292,10 +295,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
           }
           if (!issue_qk(t + 1)) break;
         }
-        if (!ret) {
-          mma_commit(smem_u32(&bars.q_empty[t & 1]));
-          continue;
-        }
+        if (!ret) continue;
         if (!mbar_wait(smem_u32(&bars.ds_ready), nret & 1, abortp, a.status)) break;
         fence_after_sync();
         // dK += dS^T Q   (A = dS^T: K-major view of the dS tile)
