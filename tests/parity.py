@@ -185,7 +185,7 @@ def decode_expected(gpu_mask, ref_o, ref_lse, ref_retained, q, k, v, scale, tau,
 
 
 def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=True, grad_dtype=torch.float32,
-                   replay=None):
+                   replay=None, legal_tiles=None):
     """gpu / ref: dicts with dq, dk, dv (numpy, BSHD) and mask / retained,
     legal, margin ([B, H, Tr, Tc]).  ``dq_rows`` / ``dk_rows`` restrict the
     comparison to boolean masks [B, L, H] / [B, L, Hkv] (sampled checks).
@@ -213,7 +213,10 @@ def check_backward(gpu, ref, block, fp32, dq_rows=None, dk_rows=None, causal=Tru
     REPLAY_STATS["bwd_replayed_tiles"] += int(diff.sum())
     if diff.any():
         assert replay is not None, "the GPU decided backward tiles differently and no replay was given"
-        assert diff.sum() <= max(1, MAX_FLIPPED_FRACTION * ref["legal"].sum())
+        # a sanity cap before the replay, over the whole call (``legal_tiles``:
+        # the legal tiles of every sequence of a packed call checked in slices)
+        n_legal = ref["legal"].sum() if legal_tiles is None else legal_tiles
+        assert diff.sum() <= max(1, MAX_FLIPPED_FRACTION * n_legal)
         ref = replay()
         bad = (gmask != ref["retained"]) & ref["legal"]
         if bad.any():

@@ -132,6 +132,15 @@ def test_decode_varlen_bf16(tau):
     _check(cfg, 1500, 6, tau, 4, 128, 61, lens=[1, 77, 128, 129, 1000, 1500])
 
 
+def test_decode_varlen_full_size():
+    """Batch 8 over caches padded to 131072 rows, lengths from one row to the
+    full cache (ragged tails, a split boundary, one token past a tile), 16
+    splits; sequences 1, 4 and 7 compared with the oracle."""
+    cfg = synthetic.CONFIGS["decode_128k"]
+    lens = [131072, 100003, 65536, 4097, 1, 128, 129, 77777]
+    _check(cfg, cfg.N, cfg.B, 1.0, cfg.num_splits, cfg.block, cfg.seed, batches=[1, 4, 7], lens=lens)
+
+
 def test_decode_varlen_fp32_d64():
     """The CUDA-core split kernel (fp32, head_dim 64, 64-key tiles)."""
     cfg = synthetic.CONFIGS["decode_128k"]

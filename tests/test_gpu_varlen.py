@@ -93,7 +93,8 @@ def _run(cfg, lens, tau, seed, heads=None, hkv=None, grad_dtype=torch.float32, c
                                        causal, forced=gm[b:b + 1, :, :t, :t].astype(bool))
             return r
 
-        parity.check_backward(gb, rb, block, fp32, causal=causal, grad_dtype=grad_dtype, replay=replay)
+        parity.check_backward(gb, rb, block, fp32, causal=causal, grad_dtype=grad_dtype, replay=replay,
+                              legal_tiles=int(refb["legal"].sum()))
         legal = np.tril(np.ones((t, t), bool)) if causal else np.ones((t, t), bool)
         np.testing.assert_array_equal(bcounts[b, :, :t], (gm[b, :, :t, :t].astype(bool) & legal).sum(-2))
 
@@ -109,6 +110,16 @@ def test_varlen_bf16_ragged(tau):
 def test_varlen_bf16_gqa_and_bf16_grads():
     cfg = synthetic.PrefillConfig("vgqa", 1, 4, 2, 700, 128, 128, torch.bfloat16, 3, (4.0,), 3.0, 0.01)
     _run(cfg, [200, 700, 64], 1.0, 73, grad_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("lens,heads,hkv,tau", [([4133, 2048, 129, 1, 700], 4, 4, 1.0),
+                                                 ([3000, 1500, 257], 8, 2, 4.0)])
+def test_varlen_medium_lengths(lens, heads, hkv, tau):
+    """Packed sequences of thousands of tokens (many tiles each, ragged tails,
+    a one-token sequence), MHA and grouped heads; every sequence compared in
+    full with the oracle."""
+    cfg = synthetic.CONFIGS["prefill_8k"]
+    _run(cfg, lens, tau, 81, heads=heads, hkv=hkv)
 
 
 def test_varlen_noncausal():
