@@ -188,7 +188,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     mbar_init(smem_u32(&bars.do_full), 1);
     mbar_init(smem_u32(&bars.s_full), 1);
     mbar_init(smem_u32(&bars.dec), 1);
-    mbar_init(smem_u32(&bars.p_ready), 1);
+    mbar_init(smem_u32(&bars.p_ready), kMath / 32);   // one arrival per math warp
     mbar_init(smem_u32(&bars.dp_full), 1);
     mbar_init(smem_u32(&bars.ds_ready), 1);
     mbar_init(smem_u32(&bars.dq_full), 1);
@@ -528,8 +528,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
       tmem_st32(lane_addr + region(t) + 64 * cg, pk);   // inside this group's own S columns
       tmem_st_wait();
       fence_before_sync();
-      if (named_vote_or(1, kMath, !ok || *abortp)) break;
-      if (tid == 0) mbar_arrive(smem_u32(&bars.p_ready));
+      // each warp hands its P^T over as soon as its own stores have landed; an
+      // abort is caught at the dS vote, and the waits before it return at once
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.p_ready));
       // the previous retained tile's dQ is read out while dV and dP^T run; the
       // MMA warp waits for it only before the next scores go into its region
       if (nret > flushed) {
