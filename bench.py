@@ -20,6 +20,7 @@ import json
 import math
 import multiprocessing as mp
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -57,11 +58,20 @@ def _args():
     return p.parse_args()
 
 
+def code_sha1(text):
+    """sha1 of a CUDA / C++ source's code: comments (// to the end of a line,
+    /* ... */ blocks), trailing blanks and empty lines removed, so that an edit
+    of the comments alone leaves it unchanged."""
+    import hashlib
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return hashlib.sha1("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def _traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` on `workload` from a recorded ncu
     capture (profiles/traffic.json), or None when there is no record or the
-    kernel's source has changed since the counters were taken."""
-    import hashlib
+    kernel's code has changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -69,7 +79,7 @@ def _traffic(kernel, workload):
     if not rec:
         return None
     src = os.path.join(ROOT, "mass_adaptive_sparse_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+    if not os.path.exists(src) or code_sha1(open(src).read()) != rec["code_sha1"]:
         return None
     return rec["bytes_per_launch"]
 

@@ -36,18 +36,27 @@ def test_decode_bytes_closed_form():
 
 
 def test_traffic_records_follow_their_sources():
-    """A record counts only while its kernel's source is the one it was taken
+    """A record counts only while its kernel's code is the one it was taken
     on: current records give their bytes, stale ones give None."""
-    import hashlib
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
     for kernel, by_workload in rec.items():
         if kernel.startswith("_"):
             continue
         for workload, r in by_workload.items():
             src = os.path.join(bench.ROOT, "mass_adaptive_sparse_gb300", "csrc", r["source"])
-            current = hashlib.sha1(open(src, "rb").read()).hexdigest() == r["source_sha1"]
+            current = bench.code_sha1(open(src).read()) == r["code_sha1"]
             assert bench._traffic(kernel, workload) == (r["bytes_per_launch"] if current else None)
     assert bench._traffic("no_such_kernel", "prefill_128k") is None
+
+
+def test_code_hash_ignores_comments_only():
+    """Comments, trailing blanks and empty lines do not change the code hash;
+    any change to the code does."""
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    same = "/* a header\n   comment */\nint f(int x) {   \n\n  return x + 1;\n}  // end\n"
+    other = "int f(int x) {\n  return x + 2;  // one more\n}\n"
+    assert bench.code_sha1(code) == bench.code_sha1(same)
+    assert bench.code_sha1(code) != bench.code_sha1(other)
 
 
 class _Done:
