@@ -26,9 +26,15 @@
 // [64,96)), dP^T (after dV has read P^T) and dQ^T (after the math warps have
 // read dP^T); then [256,384) dV and [384,512) dK.  The next tile's scores go
 // into the other region as soon as the dQ^T left there has been read out, so
-// neither dP^T nor the scores wait for the dQ hand-off of the tile before.  dS is written to shared memory once, in the
-// 128-byte-swizzled layout that is K-major for dK = dS^T Q (A = dS^T) and
-// MN-major for dQ = dS K (A = dS).
+// neither dP^T nor the scores wait for the dQ hand-off of the tile before.
+// dS is written to shared memory once, in the 128-byte-swizzled layout that
+// is K-major for dK = dS^T Q (A = dS^T) and MN-major for dQ = dS K (A = dS).
+//
+// Hand-offs to the MMA warp are made as early as each can be: thread 0
+// publishes a tile's decision right after the vote (its mask and counter
+// bookkeeping come after), each math warp signals its part of P^T once its
+// own TMEM stores have landed, and a skipped tile's Q slot goes back to the
+// producer at the decision.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
