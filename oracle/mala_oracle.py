@@ -24,12 +24,13 @@ Conventions (one head at a time; the *_bshd wrappers loop over batch/heads):
 
 Readings of points the pages leave open:
   * only key blocks with at least one legal entry for the query block are
-    visited (Algorithm 1 loops over all j; App. A.1 says "legal key blocks");
+    visited (Algorithm 1 loops over all j; App. A.1 walks only the legal ones);
   * rows (or entries) that are out of range or fully masked in a tile do not
     constrain the test (§2.2 text after Eq. 3 and after Eq. 4);
   * the skip test is a strict "<"; equality retains;
   * l = 0 is an explicit "+inf ratio, retain" branch (§2.2, first-tile rule);
-  * tau = 0 runs no test at all (dense, §2.3 "tau -> 0 recovers FullAttn");
+  * tau = 0 runs no test at all (dense: §2.3 notes that the tau -> 0 limit
+    is full attention);
   * decode: the query block is the group of query heads sharing one KV head,
     the split partition is num_splits equal ranges of whole tiles, tiles are
     visited newest to oldest inside a split, and L = N_k (§2.1, App. A.1).
@@ -148,9 +149,9 @@ def dense_attention_grads(q, k, v, do, scale, causal=True):
 
 
 def restricted_attention(q, k, v, scale, keep, bq, bk, causal=True, rows=None):
-    """Softmax attention renormalised over the kept tiles only (§2.2: "the
-    final output is ordinary softmax attention renormalized over the retained
-    tiles").  keep[i, j] says whether tile (query block i, key block j) is kept.
+    """Softmax attention renormalised over the kept tiles only (§2.2: MALA's
+    output equals plain softmax attention over the retained tiles, normalised
+    over them).  keep[i, j] says whether tile (query block i, key block j) is kept.
     Written directly as a masked softmax, with no online update.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -738,8 +739,8 @@ def matched_work_allocation(counts, scope):
 
 
 def top_mass_keep(mass, n_keep, legal):
-    """The controls' selection (App. C.2: "each control retains the
-    highest-mass candidate regions"): for query block i keep the n_keep[i]
+    """The controls' selection (App. C.2: a control keeps the candidate
+    regions of largest reference mass): for query block i keep the n_keep[i]
     legal tiles of largest reference mass; equal masses prefer the newer
     (higher) tile.  Returns [Tr, Tc] bool."""
     mass = _f64(mass)
