@@ -509,7 +509,7 @@ def main():
 
         e2e_step()
         barrier()
-        n_e2e = max(1, min(args.steps, 5))
+        n_e2e = max(1, min(args.steps, 10))
         es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
         es[0].record(stream)
         for i in range(n_e2e):
