@@ -92,6 +92,28 @@ def test_bwd_rejects_small_workspace(lib):
     assert lib.mala_bwd(*([None] + args[1:]), FAKE, 1 << 20, None, None, None) == 1
 
 
+def _bwd(lib, ptr=None, ptr_at=None, B=1, L=256, Hq=2, Hkv=2, D=64, dt=1, gdt=1, causal=1, blk=64, tau=1.0,
+         scale=0.125, ws=FAKE, ws_bytes=1 << 30):
+    ptrs = [FAKE] * 9                  # q, k, v, o, dO, lse, dQ, dK, dV
+    if ptr_at is not None:
+        ptrs[ptr_at] = ptr
+    return lib.mala_bwd(*ptrs, B, L, L, Hq, Hkv, D, dt, gdt, causal, blk, blk, tau, scale, ws, ws_bytes,
+                        None, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    *[(dict(ptr=None, ptr_at=i), 1) for i in range(9)],
+    *[(dict(ptr=MISALIGNED, ptr_at=i), 1) for i in range(9)],
+    (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(dt=7), 1), (dict(gdt=7), 1), (dict(causal=2), 1),
+    (dict(tau=-1.0), 1), (dict(tau=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(D=96), 2), (dict(blk=32), 2),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, code):
+    """Every pointer (null or misaligned) and the shared shape checks, before
+    the workspace is looked at."""
+    assert _bwd(lib, **kw) == code
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(splits=0), 1), (dict(splits=300), 1), (dict(Hq=12, Hkv=8), 1), (dict(Hq=48, Hkv=3), 2),
     (dict(D=80), 2), (dict(blk=32), 2), (dict(tau=-0.5), 1), (dict(ws=None), 3), (dict(ws_bytes=64), 3),
