@@ -142,6 +142,21 @@ def test_device_status_rejects_null(lib):
     assert lib.mala_device_status(None, None) == 1
 
 
+@pytest.mark.parametrize("cu,batch,total,lmax", [
+    (None, 2, 512, 256), (ctypes.c_void_p(0x10002), 2, 512, 256), (FAKE, 0, 512, 256),
+    (FAKE, 2, 0, 256), (FAKE, 2, 512, 0), (FAKE, 2, 512, 513),
+])
+def test_packed_prefill_rejects_bad_sequence_bounds(lib, cu, batch, total, lmax):
+    """cu_seqlens null or misaligned, no sequence, no token, or a longest
+    sequence of 0 or past the packed total: both packed entry points refuse
+    before any launch."""
+    fwd = lib.mala_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, cu, batch, total, lmax, 2, 2, 64, 1, 1, 1, 64, 64,
+                              1.0, 0.125, None, None, None)
+    bwd = lib.mala_bwd_varlen(*([FAKE] * 9), cu, batch, total, lmax, 2, 2, 64, 1, 1, 1, 64, 64, 1.0, 0.125,
+                              FAKE, 1 << 30, None, None, None)
+    assert fwd == 1 and bwd == 1
+
+
 def test_decode_varlen_rejects_missing_or_misaligned_lengths(lib):
     args = [FAKE] * 5
     shape = [8, 1024, 32, 8, 128, 0, 0, 128, 16, 1.0, 0.08, FAKE, 1 << 30, None, None, None]
